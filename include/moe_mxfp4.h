@@ -1,0 +1,177 @@
+/*
+ * moe_mxfp4.h — C ABI of the routed MXFP4 mixture-of-experts layer on GB300
+ * (sm_103a), exported by libmoe_mxfp4.so.
+ *
+ * The layer (per token t, hidden size H, E experts, top-k routing, expert
+ * intermediate size I):
+ *
+ *   s[t][e]  = sum_h x[t][h] * Wr[e][h] + b[e]                 router scores
+ *   ids[t]   = the k largest s[t][.], descending, ties to the lower index
+ *   w[t][j]  = exp(s_j - s_0) / sum_i exp(s_i - s_0)           over the k
+ *   y[t][j]  = Wd_e (silu(Wg_e x_t) * (Wu_e x_t)),  e = ids[t][j]
+ *   out[t]   = (accumulate ? out[t] : 0) + sum_{j=0}^{k-1} w[t][j] y[t][j]
+ *              (+ an optional always-on bf16 shared expert, weight 1)
+ *
+ * Where the definition comes from:
+ *   - one layer routes each token to 16 of 896 experts whose weights are MXFP4
+ *     [deltafin, "How it splits the model"];
+ *   - the provider hands back an authoritative top-16 "route mailbox" of ids
+ *     and fp32 weights whose route order and weight bits are checked at every
+ *     ABI transition [Deltafin's custom compiled runtime, "Complete target
+ *     sequence tape"]; a trace of it records the 16 ids and fp32 weight bits
+ *     [How the native runtime works, "Router tracing and offline expert
+ *     warming"];
+ *   - the MXFP4 experts are used unchanged, activations stay fp32, all 16
+ *     selected experts run [Deltafin's custom compiled runtime, "Weight
+ *     fidelity"];
+ *   - each expert is six tensors (gate, up, down; nibbles and E8M0 scales)
+ *     [deltafin, "The techniques that bought the 82x"]; experts may sit in
+ *     scattered spans that the provider accepts without a copy [Deltafin's
+ *     custom compiled runtime, "Exact next-layer expert prefetch"], hence the
+ *     per-expert descriptor table below;
+ *   - a small versioned C ABI, descriptor-driven binding, failures fail closed
+ *     [Deltafin's custom compiled runtime, "Production ownership", "Coarse
+ *     provider binding", "Configuration and device selection"].
+ * The router nonlinearity, the SwiGLU activation, the nibble order and the
+ * block axis are not on those pages; this library takes: softmax over the
+ * selected scores; silu(z) = z / (1 + e^-z); element 2i of a block is the low
+ * nibble of byte i; blocks of 32 run along the contraction axis.
+ *
+ * MXFP4 matrix (moe_mx_mat) with R rows and C columns (C % 32 == 0):
+ *   q: uint8 [R][C/2]   E2M1 codes, element 2i low nibble, 2i+1 high nibble
+ *   s: uint8 [R][C/32]  E8M0 scales, value 2^(s-127), 255 = NaN
+ *   element (r, c) = e2m1(code) * 2^(s[r][c/32] - 127),
+ *   e2m1 codes: {0, .5, 1, 1.5, 2, 3, 4, 6}, bit 3 = sign (OCP MX v1.0).
+ * Expert e: gate and up are [I][H] (rows = intermediate features), down is
+ * [H][I] (rows = hidden features).
+ *
+ * Conventions for every call:
+ *   - Memory: every data pointer is a DEVICE pointer owned by the caller; the
+ *     library allocates nothing and keeps no pointer after the call returns
+ *     (work is enqueued on `stream`, so buffers must stay valid until it has
+ *     run).  `shape` and `shared` point to HOST structs; `experts` points to a
+ *     DEVICE array of E moe_expert descriptors.
+ *   - Alignment: x, q tensors, out, ws: 16 bytes; everything else: its
+ *     element size.  Misalignment is MOE_ERR_INVALID_ARG.
+ *   - Asynchrony: calls enqueue kernels on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and return; there is no host synchronisation
+ *     except in moe_device_status().  The calls make no CUDA allocation.
+ *   - Errors: argument problems are reported before anything is launched
+ *     (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE); a launch
+ *     failure returns MOE_ERR_CUDA.  Problems the kernels detect (an expert id
+ *     out of range, a bounded wait that gave up, a range overflow in the fp16
+ *     operands of the prefill path) set a status word inside `ws` that
+ *     moe_device_status() reads; outputs of such a call are unspecified.
+ *   - Workspace: `ws` must hold moe_workspace_bytes(shape) bytes; its contents
+ *     need not be initialised and are overwritten.  One workspace must not be
+ *     used by two calls that may run concurrently.
+ *   - Limits: 1 <= T <= 65536, 32 <= H <= 16384, 32 <= I <= 8192, H % 32 ==
+ *     I % 32 == 0, 1 <= k <= min(E, 32), k * (I/32) <= 1024, E <= 65536.
+ *     fp32 activations are accepted on the decode path (T <= 64); the prefill
+ *     path takes bf16 activations.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1u
+
+/* Status codes returned by every call (and stored in the device status word). */
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad shape, bad enum */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid request outside this build's limits */
+  MOE_ERR_WORKSPACE = 3,    /* ws_bytes < moe_workspace_bytes(shape) */
+  MOE_ERR_CUDA = 4,         /* a CUDA launch or query failed */
+  MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
+  MOE_ERR_DEVICE_CHECK = 6, /* device: an expert id out of [0, E) */
+  MOE_ERR_RANGE = 7         /* device: a prefill fp16 operand overflowed */
+} moe_status;
+
+/* Activation element types. */
+typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
+
+/* Expert execution path. */
+typedef enum {
+  MOE_PATH_AUTO = 0,    /* decode for T <= 64 or fp32 activations, else prefill */
+  MOE_PATH_DECODE = 1,  /* weight-streaming MXFP4 GEMV on CUDA cores (T <= 64) */
+  MOE_PATH_PREFILL = 2  /* grouped MXFP4 GEMM on tcgen05 tensor cores (bf16 x) */
+} moe_path;
+
+#define MOE_DECODE_MAX_T 64
+
+typedef struct { const uint8_t* q; const uint8_t* s; } moe_mx_mat;   /* see above */
+typedef struct { moe_mx_mat gate, up, down; } moe_expert;            /* six tensors */
+typedef struct { const uint16_t *gate, *up, *down; } moe_dense_bf16; /* bf16 bits */
+typedef struct { int32_t T, H, E, I, k; } moe_shape;
+
+/* MOE_ABI_VERSION of the loaded library. */
+uint32_t moe_abi_version(void);
+
+/* Static English text for a status code (never NULL). */
+const char* moe_status_string(int status);
+
+/* Bytes of device workspace every call on this shape needs (0 if the shape is
+ * invalid).  The same workspace serves moe_route, moe_mxfp4_experts and
+ * moe_forward. */
+size_t moe_workspace_bytes(const moe_shape* shape);
+
+/* Routing only: router scores, top-k with renormalised fp32 weights, and the
+ * bucket layout of a counting sort by expert.
+ *   x         [T][H] activations of type x_dtype (MOE_DT_F32 / MOE_DT_BF16)
+ *   w_router  [E][H] fp32;  b_router [E] fp32 or NULL (added to the scores)
+ *   ids       [T][k] int32 out, descending score, ties to the lower index
+ *   w         [T][k] fp32  out, softmax of the selected scores
+ *   offsets   [E+1] int32 out or NULL: offsets[e] = number of (t, j) pairs
+ *             routed to experts below e; offsets[E] = T*k
+ *   sorted_idx[T*k] int32 out or NULL: flat pairs t*k+j grouped by expert,
+ *             ascending (t, j) inside each expert (stable)
+ * [Deltafin's custom compiled runtime, "Complete target sequence tape";
+ *  "Exact next-layer expert prefetch": the final expert array is ordered by
+ *  the real route union.] */
+int moe_route(const moe_shape* shape, const void* x, int x_dtype, const float* w_router,
+              const float* b_router, int32_t* ids, float* w, int32_t* offsets, int32_t* sorted_idx,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Experts only, given routes (as moe_route produces them):
+ *   out[t] = (accumulate ? out[t] : 0) + sum_j w[t][j] * y_{ids[t][j]}(x_t)
+ *   experts   device array [E] of descriptors (gate/up [I][H], down [H][I])
+ *   offsets, sorted_idx: the bucket layout of ids, or both NULL (then it is
+ *             rebuilt in ws from ids)
+ *   out       [T][H] fp32
+ *   path      moe_path
+ * The decode path sums the k expert outputs of a token in slot order and is
+ * bitwise independent of the other tokens in the batch; the prefill path adds
+ * them with fp32 atomics (order not fixed).
+ * [deltafin, "The techniques that bought the 82x": fused MXFP4 dequant+GEMV;
+ *  Deltafin's custom compiled runtime, "The native build": ordered reduction.] */
+int moe_mxfp4_experts(const moe_shape* shape, const void* x, int x_dtype, const moe_expert* experts,
+                      const int32_t* ids, const float* w, const int32_t* offsets, const int32_t* sorted_idx,
+                      float* out, int accumulate, int path, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer: moe_route then moe_mxfp4_experts, plus the optional shared
+ * expert (shared == NULL for none; host struct of device bf16 pointers, gate/up
+ * [I][H], down [H][I], added with weight 1).  ids_out [T][k] / w_out [T][k]
+ * receive the route when non-NULL. */
+int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float* w_router,
+                const float* b_router, const moe_expert* experts, const moe_dense_bf16* shared, float* out,
+                int accumulate, int32_t* ids_out, float* w_out, int path, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* Synchronises `stream`, then reads the device status word of `ws` into
+ * *status_out (MOE_OK if no kernel flagged a problem since the last call that
+ * began with this workspace).  Returns MOE_ERR_CUDA if the synchronisation or
+ * the copy fails. */
+int moe_device_status(const void* ws, void* stream, int* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_MXFP4_H */

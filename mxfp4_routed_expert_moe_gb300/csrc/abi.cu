@@ -1,0 +1,222 @@
+// abi.cu — the exported C entry points: argument validation, workspace
+// layout, and the launch sequence of each call.  Nothing here allocates or
+// synchronises except moe_device_status().
+#include <string.h>
+
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int validate_shape(const moe_shape* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 1 || s->H < 32 || s->I < 32 || s->E < 1 || s->k < 1) return MOE_ERR_INVALID_ARG;
+  if (s->H % 32 != 0 || s->I % 32 != 0 || s->k > s->E) return MOE_ERR_INVALID_ARG;
+  if (s->k > kMaxK || s->T > 65536 || s->H > 16384 || s->I > 8192 || s->E > 65536) return MOE_ERR_UNSUPPORTED;
+  if (s->k * (s->I / 32) > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)s->T * s->k > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(*s, nullptr).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool decode_experts_supported(const moe_shape* s) {
+  // Decode gate/up keeps one block column per thread (H <= 8192); down keeps
+  // one block column per thread in groups (I <= 12288 already implied).
+  return s->T <= kDecodeMaxT && s->H <= 8192;
+}
+
+// Resolve MOE_PATH_AUTO and check the chosen path's limits.
+int resolve_path(const moe_shape* s, int x_dtype, int path, int* out) {
+  if (path == MOE_PATH_AUTO) path = (s->T <= kDecodeMaxT || x_dtype == MOE_DT_F32) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  if (path == MOE_PATH_DECODE) {
+    if (!decode_experts_supported(s)) return MOE_ERR_UNSUPPORTED;
+  } else if (path == MOE_PATH_PREFILL) {
+    if (x_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  *out = path;
+  return MOE_OK;
+}
+
+BucketParams bucket_params(const moe_shape* s, const int32_t* ids, int32_t* offsets_out, int32_t* sorted_out,
+                           const Ws& ws) {
+  BucketParams b;
+  b.T = s->T; b.E = s->E; b.k = s->k;
+  b.ids = ids;
+  b.offsets_out = offsets_out;
+  b.sorted_out = sorted_out;
+  b.n_tile = kPfNTile;
+  b.m_tiles_gu = (s->I + kPfMTile - 1) / kPfMTile;
+  b.m_tiles_dn = (s->H + kPfMTile - 1) / kPfMTile;
+  b.ws = ws;
+  return b;
+}
+
+int do_route(const moe_shape* s, const void* x, int x_dtype, const float* wr, const float* br, int32_t* ids, float* w,
+             int32_t* offsets, int32_t* sorted, const Ws& ws, bool want_decode_route, cudaStream_t st) {
+  RouteParams p;
+  p.T = s->T; p.H = s->H; p.E = s->E; p.k = s->k;
+  p.x = x;
+  p.x_bf16 = x_dtype == MOE_DT_BF16;
+  p.wr = wr;
+  p.br = br;
+  p.ids = ids;
+  p.w = w;
+  p.offsets = offsets;
+  p.sorted = sorted;
+  p.want_buckets = 1;
+  p.ws = ws;
+  if (want_decode_route && route_decode_supported(s->T, s->H, s->E, s->k)) return cuda_status(launch_route_decode(p, st));
+  return cuda_status(launch_route_prefill(p, bucket_params(s, ids, offsets, sorted, ws), st));
+}
+
+ExpertParams expert_params(const moe_shape* s, const void* x, int x_dtype, const moe_expert* experts,
+                           const int32_t* ids, const float* w, const int32_t* offsets, const int32_t* sorted,
+                           float* out, int accumulate, const moe_dense_bf16* shared, const Ws& ws) {
+  ExpertParams p;
+  memset(&p, 0, sizeof p);
+  p.T = s->T; p.H = s->H; p.E = s->E; p.I = s->I; p.k = s->k;
+  p.x = x;
+  p.x_bf16 = x_dtype == MOE_DT_BF16;
+  p.experts = experts;
+  p.ids = ids;
+  p.w = w;
+  p.offsets = offsets;
+  p.sorted = sorted;
+  p.out = out;
+  p.accumulate = accumulate ? 1 : 0;
+  if (shared) {
+    p.sh_gate = shared->gate;
+    p.sh_up = shared->up;
+    p.sh_down = shared->down;
+  }
+  p.ws = ws;
+  return p;
+}
+
+int run_experts(const ExpertParams& p, int path, cudaStream_t st) {
+  if (path == MOE_PATH_DECODE) {
+    if (p.sh_gate) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_decode_experts(p, st));
+  }
+  return cuda_status(launch_prefill_experts(p, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad shape or enum)";
+    case MOE_ERR_UNSUPPORTED: return "request outside the supported limits of this build";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_bytes(shape)";
+    case MOE_ERR_CUDA: return "a CUDA launch or query failed";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case MOE_ERR_DEVICE_CHECK: return "device check failed: expert id or bucket entry out of range";
+    case MOE_ERR_RANGE: return "prefill fp16 operand out of range";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+  if (validate_shape(shape) != MOE_OK) return 0;
+  return ws_layout(*shape, nullptr).total;
+}
+
+int moe_route(const moe_shape* shape, const void* x, int x_dtype, const float* w_router, const float* b_router,
+              int32_t* ids, float* w, int32_t* offsets, int32_t* sorted_idx, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (!x || !w_router || !ids || !w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(ids, 4) || !aligned(w, 4)) return MOE_ERR_INVALID_ARG;
+  if ((b_router && !aligned(b_router, 4)) || (offsets && !aligned(offsets, 4)) || (sorted_idx && !aligned(sorted_idx, 4)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const Ws L = ws_layout(*shape, ws);
+  if ((st = cuda_status(cudaMemsetAsync(L.hdr, 0, sizeof(WsHeader), s))) != MOE_OK) return st;
+  return do_route(shape, x, x_dtype, w_router, b_router, ids, w, offsets, sorted_idx, L, shape->T <= kDecodeMaxT, s);
+}
+
+int moe_mxfp4_experts(const moe_shape* shape, const void* x, int x_dtype, const moe_expert* experts,
+                      const int32_t* ids, const float* w, const int32_t* offsets, const int32_t* sorted_idx,
+                      float* out, int accumulate, int path, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (!x || !experts || !ids || !w || !out) return MOE_ERR_INVALID_ARG;
+  if ((offsets == nullptr) != (sorted_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(experts, 8) || !aligned(ids, 4) || !aligned(w, 4))
+    return MOE_ERR_INVALID_ARG;
+  int rpath;
+  if ((st = resolve_path(shape, x_dtype, path, &rpath)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const Ws L = ws_layout(*shape, ws);
+  if ((st = cuda_status(cudaMemsetAsync(L.hdr, 0, sizeof(WsHeader), s))) != MOE_OK) return st;
+  BucketParams b = bucket_params(shape, ids, nullptr, nullptr, L);
+  if (offsets) {
+    if ((st = cuda_status(launch_plan_from_offsets(b, offsets, s))) != MOE_OK) return st;
+  } else {
+    if ((st = cuda_status(launch_bucket_from_ids(b, s))) != MOE_OK) return st;
+    offsets = L.offsets;
+    sorted_idx = L.sorted;
+  }
+  const ExpertParams p = expert_params(shape, x, x_dtype, experts, ids, w, offsets, sorted_idx, out, accumulate, nullptr, L);
+  return run_experts(p, rpath, s);
+}
+
+int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float* w_router, const float* b_router,
+                const moe_expert* experts, const moe_dense_bf16* shared, float* out, int accumulate, int32_t* ids_out,
+                float* w_out, int path, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_shape(shape);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(shape, ws, ws_bytes)) != MOE_OK) return st;
+  if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (!x || !w_router || !experts || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(out, 16) || !aligned(experts, 8)) return MOE_ERR_INVALID_ARG;
+  if ((b_router && !aligned(b_router, 4)) || (ids_out && !aligned(ids_out, 4)) || (w_out && !aligned(w_out, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (shared && (!shared->gate || !shared->up || !shared->down || !aligned(shared->gate, 16) ||
+                 !aligned(shared->up, 16) || !aligned(shared->down, 16)))
+    return MOE_ERR_INVALID_ARG;
+  int rpath;
+  if ((st = resolve_path(shape, x_dtype, path, &rpath)) != MOE_OK) return st;
+  if (rpath == MOE_PATH_DECODE && shared) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  const Ws L = ws_layout(*shape, ws);
+  int32_t* ids = ids_out ? ids_out : L.ids;
+  float* w = w_out ? w_out : L.w;
+  if ((st = cuda_status(cudaMemsetAsync(L.hdr, 0, sizeof(WsHeader), s))) != MOE_OK) return st;
+  if ((st = do_route(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L, rpath == MOE_PATH_DECODE, s)) != MOE_OK)
+    return st;
+  const ExpertParams p = expert_params(shape, x, x_dtype, experts, ids, w, L.offsets, L.sorted, out, accumulate, shared, L);
+  return run_experts(p, rpath, s);
+}
+
+int moe_device_status(const void* ws, void* stream, int* status_out) {
+  if (!ws || !status_out) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  *status_out = (int)v;
+  return MOE_OK;
+}
+
+}  // extern "C"

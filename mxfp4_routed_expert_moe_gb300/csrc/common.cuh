@@ -1,0 +1,263 @@
+// common.cuh — shared device helpers, workspace layout and kernel parameter
+// blocks of the routed MXFP4 MoE library (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe_mxfp4.h"
+
+namespace moe {
+
+constexpr int kDecodeMaxT = MOE_DECODE_MAX_T;
+constexpr int kMaxK = 32;
+constexpr int kNumSMs = 152;  // GB300; launch code queries the device instead
+
+// ---------------------------------------------------------------- workspace --
+// Header at the start of the workspace (zeroed at the start of every call).
+struct WsHeader {
+  uint32_t status;      // first nonzero moe_status a kernel recorded
+  uint32_t ticket;      // last-block-done counter of the bucket count kernel
+  uint32_t n_active;    // number of experts with at least one routed pair
+  uint32_t route_ticket;
+  uint32_t queue[16];   // work counters of persistent kernels
+  uint32_t pad[44];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+enum Queue { kQGateUp = 0, kQDown = 1, kQPfGateUp = 2, kQPfDown = 3, kQShared = 4, kQSharedDown = 5 };
+
+// Device pointers into one workspace.
+struct Ws {
+  WsHeader* hdr;
+  float2* logits;       // [T][E] router scores as (hi, lo) double-floats
+  int32_t* ids;         // [T][k]  (used when the caller gives none)
+  float* w;             // [T][k]
+  uint32_t* mask;       // [E][W]  W = ceil(T/32): token bitmask per expert
+  int32_t* wprefix;     // [E][W]  exclusive popcount prefix of mask words
+  int32_t* offsets;     // [E+1]
+  int32_t* sorted;      // [T*k]
+  int32_t* act_e;       // [E]     active experts, ascending
+  int32_t* act_pref_gu; // [E+1]   prefix of prefill gate/up tiles per active expert
+  int32_t* act_pref_dn; // [E+1]   prefix of prefill down tiles per active expert
+  uint16_t* xh;         // [T][H]  fp16 activations (prefill)
+  float* xscale;        // [T]     2^-sigma_t of the fp16 activations
+  void* h;              // [T*k][I] fp32 (decode) or fp16 (prefill)
+  float* y;             // [T*k][H] fp32 (decode, T <= 64)
+  uint32_t* rowdone;    // [ceil(H/32)] per-row-tile completion counters
+  size_t total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Layout of the workspace for a shape; pointers are offsets from `base`.
+inline Ws ws_layout(const moe_shape& s, void* base) {
+  const size_t T = (size_t)s.T, H = (size_t)s.H, E = (size_t)s.E, I = (size_t)s.I, k = (size_t)s.k;
+  const size_t W = (T + 31) / 32;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return (char*)base + o;
+  };
+  Ws ws;
+  ws.hdr = (WsHeader*)take(sizeof(WsHeader));
+  ws.logits = (float2*)take(T * E * 8);
+  ws.ids = (int32_t*)take(T * k * 4);
+  ws.w = (float*)take(T * k * 4);
+  ws.mask = (uint32_t*)take(E * W * 4);
+  ws.wprefix = (int32_t*)take(E * W * 4);
+  ws.offsets = (int32_t*)take((E + 1) * 4);
+  ws.sorted = (int32_t*)take(T * k * 4);
+  ws.act_e = (int32_t*)take(E * 4);
+  ws.act_pref_gu = (int32_t*)take((E + 1) * 4);
+  ws.act_pref_dn = (int32_t*)take((E + 1) * 4);
+  ws.xh = (uint16_t*)take(T * H * 2);
+  ws.xscale = (float*)take(T * 4);
+  const size_t Td = T < (size_t)kDecodeMaxT ? T : (size_t)kDecodeMaxT;
+  // h: fp32 for the decode path (Td*k rows), fp16 for the prefill path (T*k rows).
+  const size_t h_dec = Td * k * I * 4, h_pf = T * k * I * 2;
+  ws.h = (void*)take(h_dec > h_pf ? h_dec : h_pf);
+  ws.y = (float*)take(Td * k * H * 4);
+  ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
+  ws.total = off;
+  return ws;
+}
+
+// ------------------------------------------------------------- device utils --
+__device__ __forceinline__ void set_status(WsHeader* hdr, uint32_t st) {
+  atomicCAS(&hdr->status, 0u, st);
+}
+
+// E8M0 scale byte -> fp32 2^(s-127); s = 0 gives the subnormal 2^-127, s = 255 NaN.
+__device__ __forceinline__ float e8m0_f32(uint32_t s) {
+  uint32_t bits = s == 0u ? 0x00400000u : (s << 23);
+  bits = s == 255u ? 0x7FC00000u : bits;
+  return __uint_as_float(bits);
+}
+
+// Two E2M1 codes (low byte of v: element 0 in bits 3..0, element 1 in 7..4)
+// -> f16x2 (element 0 in the low half).  Exact: every E2M1 value is an fp16.
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t v, int byte) {
+  uint32_t r;
+  switch (byte) {
+    case 0: asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}" : "=r"(r) : "r"(v)); break;
+    case 1: asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b1;\n}" : "=r"(r) : "r"(v)); break;
+    case 2: asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b2;\n}" : "=r"(r) : "r"(v)); break;
+    default: asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b3;\n}" : "=r"(r) : "r"(v)); break;
+  }
+  return r;
+}
+
+__device__ __forceinline__ float2 f16x2_f32x2(uint32_t h2) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+__device__ __forceinline__ float bf16_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Streaming 16-byte load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return (uint32_t)v;
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Sum over the 32 lanes of v[lane % V] for V values per lane (V a power of two
+// <= 32): returns, on each lane, the warp total of value index (lane & (V-1)).
+// The addition tree is the same for every value index and every V-sized
+// packing, so a value's total does not depend on what else is packed with it.
+template <int V>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[V]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = V / 2; m >= 1; m /= 2) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = upper ? v[i] : v[i + m];
+      const float keep = upper ? v[i + m] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
+    }
+  }
+#pragma unroll
+  for (int m = V; m < 32; m *= 2) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], m);
+  return v[0];
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------ double-float arithmetic --
+// A value is carried as an unevaluated sum hi + lo of two floats (Knuth's
+// TwoSum / Dekker's Fast2Sum error-free transformations), which keeps router
+// scores accurate to ~2^-44 relative: the fp32 weights derived from them do
+// not inherit fp32 rounding of large scores.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+
+// (hi, lo) += p, lo collecting the rounding errors (not renormalised).
+__device__ __forceinline__ void df_add_f(float& hi, float& lo, float p) {
+  float s, e;
+  two_sum(hi, p, s, e);
+  hi = s;
+  lo += e;
+}
+
+// (hi, lo) = (ahi, alo) + (bhi, blo), renormalised.
+__device__ __forceinline__ void df_add(float ahi, float alo, float bhi, float blo, float& hi, float& lo) {
+  float s, e;
+  two_sum(ahi, bhi, s, e);
+  e += alo + blo;
+  hi = s + e;
+  lo = e - (hi - s);
+}
+
+// Double-float version of warp_transpose_reduce (same addition tree).
+template <int V>
+__device__ __forceinline__ void warp_transpose_reduce_df(float (&vh)[V], float (&vl)[V], float& oh, float& ol) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = V / 2; m >= 1; m /= 2) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float sh = upper ? vh[i] : vh[i + m];
+      const float sl = upper ? vl[i] : vl[i + m];
+      const float kh = upper ? vh[i + m] : vh[i];
+      const float kl = upper ? vl[i + m] : vl[i];
+      const float rh = __shfl_xor_sync(0xFFFFFFFFu, sh, m);
+      const float rl = __shfl_xor_sync(0xFFFFFFFFu, sl, m);
+      df_add(kh, kl, rh, rl, vh[i], vl[i]);
+    }
+  }
+#pragma unroll
+  for (int m = V; m < 32; m *= 2) {
+    const float rh = __shfl_xor_sync(0xFFFFFFFFu, vh[0], m);
+    const float rl = __shfl_xor_sync(0xFFFFFFFFu, vl[0], m);
+    df_add(vh[0], vl[0], rh, rl, vh[0], vl[0]);
+  }
+  oh = vh[0];
+  ol = vl[0];
+}
+
+// ----------------------------------------------------------- kernel params --
+struct RouteParams {
+  int T, H, E, k;
+  const void* x;
+  int x_bf16;
+  const float* wr;
+  const float* br;
+  int32_t* ids;
+  float* w;
+  int32_t* offsets;     // bucket outputs (may alias workspace)
+  int32_t* sorted;
+  int want_buckets;
+  Ws ws;
+};
+
+// Bucketing / planning: counting sort of routed pairs by expert, the active
+// expert list and the prefill tile prefixes.
+struct BucketParams {
+  int T, E, k;
+  const int32_t* ids;      // [T][k]
+  int32_t* offsets_out;    // [E+1] caller copy or NULL
+  int32_t* sorted_out;     // [T*k] caller copy or NULL
+  int n_tile;              // prefill token tile (columns of one MMA tile)
+  int m_tiles_gu;          // prefill row tiles of gate/up (ceil(I/128))
+  int m_tiles_dn;          // prefill row tiles of down (ceil(H/128))
+  Ws ws;
+};
+
+struct ExpertParams {
+  int T, H, E, I, k;
+  const void* x;
+  int x_bf16;
+  const moe_expert* experts;  // device [E]
+  const int32_t* ids;
+  const float* w;
+  const int32_t* offsets;
+  const int32_t* sorted;
+  float* out;
+  int accumulate;
+  const moe_dense_bf16* shared_dev;  // unused on device; shared pointers below
+  const uint16_t *sh_gate, *sh_up, *sh_down;
+  Ws ws;
+};
+
+}  // namespace moe

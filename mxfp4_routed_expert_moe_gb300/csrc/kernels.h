@@ -1,0 +1,44 @@
+// kernels.h — host-side launchers of the library's kernels (one per stage).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Launch with programmatic dependent launch enabled: the kernel may start
+// while the previous kernel on the stream finishes; it must call pdl_wait()
+// before touching that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+int device_sm_count();
+
+// route.cu
+bool route_decode_supported(int T, int H, int E, int k);
+cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s);
+cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s);
+cudaError_t launch_bucket_from_ids(const BucketParams& b, cudaStream_t s);
+cudaError_t launch_plan_from_offsets(const BucketParams& b, const int32_t* offsets, cudaStream_t s);
+
+// decode.cu
+cudaError_t launch_decode_experts(const ExpertParams& p, cudaStream_t s);
+
+// prefill.cu
+constexpr int kPfNTile = 128;   // tokens per MMA tile (N)
+constexpr int kPfMTile = 128;   // weight rows per MMA tile (M)
+cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s);
+
+}  // namespace moe

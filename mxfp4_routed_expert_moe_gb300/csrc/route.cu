@@ -1,0 +1,568 @@
+// route.cu — router scores, top-k with renormalised weights, and the bucket
+// layout (counting sort by expert).
+//
+// Routing follows [Deltafin's custom compiled runtime, "Complete target
+// sequence tape"]: an authoritative top-16 route of ids and fp32 weights in a
+// fixed route order; here the order is descending score with ties to the
+// lower expert index, and the weights are the softmax of the selected scores.
+// The bucket layout groups the routed (token, slot) pairs by expert, which is
+// the order of the route union [Deltafin's custom compiled runtime, "Exact
+// next-layer expert prefetch"].
+#include <utility>
+
+#include "kernels.h"
+
+namespace moe {
+
+constexpr uint32_t kTaken = 0xFFFFFFFFu;  // hi bits of an already selected expert
+
+__device__ __forceinline__ uint32_t ord32(float f) {
+  const uint32_t b = __float_as_uint(f + 0.0f);  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);  // monotone in f
+}
+
+// Orderable key of a double-float score (hi, lo): value order, with a taken
+// entry (hi bits kTaken) below every real score.
+__device__ __forceinline__ unsigned long long score_key(float2 v) {
+  if (__float_as_uint(v.x) == kTaken) return 0ull;
+  return ((unsigned long long)ord32(v.x) << 32) | ord32(v.y);
+}
+
+// Top-k of one token by one warp over its double-float scores in shared
+// memory `row` (destroyed): larger score first, lower expert index on equal
+// scores.  Lane j < k returns slot j's expert and score.
+__device__ __forceinline__ void warp_topk(float2* row, int E, int k, int& my_e, float2& my_s) {
+  const int lane = threadIdx.x & 31;
+  my_e = -1;
+  my_s = make_float2(0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+    int best_e = 0x7FFFFFFF;
+    for (int e = lane; e < E; e += 32) {
+      const unsigned long long kk = score_key(row[e]);
+      if (kk > best) { best = kk; best_e = e; }
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, m);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, best_e, m);
+      if (ok > best || (ok == best && oe < best_e)) { best = ok; best_e = oe; }
+    }
+    if (lane == j) {
+      my_e = best_e;
+      my_s = row[best_e];
+    }
+    __syncwarp();
+    if (lane == 0) row[best_e].x = __uint_as_float(kTaken);
+    __syncwarp();
+  }
+}
+
+// Softmax of the selected scores held by lanes 0..k-1 (slot order): lane j
+// gets exp(s_j - s_0) / sum_i exp(s_i - s_0), the differences taken from the
+// double-float scores.
+__device__ __forceinline__ float warp_route_weight(float2 my_s, int k) {
+  const int lane = threadIdx.x & 31;
+  const float h0 = __shfl_sync(0xFFFFFFFFu, my_s.x, 0);
+  const float l0 = __shfl_sync(0xFFFFFFFFu, my_s.y, 0);
+  const float d = (my_s.x - h0) + (my_s.y - l0);
+  const float ex = lane < k ? expf(d) : 0.0f;
+  float z = ex;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, m);
+  return ex / z;
+}
+
+// Exclusive scan of per-expert counts (held in ws.offsets[0..E) on entry) into
+// ws.offsets (and the caller's copy), plus the active-expert list and the
+// prefill tile prefixes.  Called by every thread of one CTA.
+__device__ void plan_scan(const BucketParams& p) {
+  __shared__ int warp_tot[3][32];
+  __shared__ int carry[3];
+  const int E = p.E, tid = threadIdx.x, nthreads = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nw = nthreads >> 5;
+  if (tid < 3) carry[tid] = 0;
+  __syncthreads();
+  for (int base = 0; base < E; base += nthreads) {
+    const int e = base + tid;
+    const int c = e < E ? __ldcg(&p.ws.offsets[e]) : 0;
+    int v[3] = {c, c > 0 ? 1 : 0, c > 0 ? (c + p.n_tile - 1) / p.n_tile : 0};
+    int incl[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      incl[q] = v[q];
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl[q], m);
+        if (lane >= m) incl[q] += o;
+      }
+      if (lane == 31) warp_tot[q][warp] = incl[q];
+    }
+    __syncthreads();
+    int excl[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      int pre = carry[q];
+      for (int w = 0; w < warp; ++w) pre += warp_tot[q][w];
+      excl[q] = pre + incl[q] - v[q];
+    }
+    __syncthreads();
+    if (e < E) {
+      p.ws.offsets[e] = excl[0];
+      if (p.offsets_out) p.offsets_out[e] = excl[0];
+      if (c > 0) {
+        p.ws.act_e[excl[1]] = e;
+        p.ws.act_pref_gu[excl[1]] = excl[2] * p.m_tiles_gu;
+        p.ws.act_pref_dn[excl[1]] = excl[2] * p.m_tiles_dn;
+      }
+    }
+    if (tid == 0) {
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+        for (int w = 0; w < nw; ++w) carry[q] += warp_tot[q][w];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.ws.offsets[E] = carry[0];
+    if (p.offsets_out) p.offsets_out[E] = carry[0];
+    p.ws.hdr->n_active = (uint32_t)carry[1];
+    p.ws.act_pref_gu[carry[1]] = carry[2] * p.m_tiles_gu;
+    p.ws.act_pref_dn[carry[1]] = carry[2] * p.m_tiles_dn;
+  }
+}
+
+// ------------------------------------------------------ decode router GEMV --
+// s[t][e] = sum_h x[t][h] * Wr[e][h] (+ b[e]) for T <= 64, H <= 8192.  Each CTA
+// owns 4 rows of Wr and walks the tokens in pairs; thread tau holds the
+// activations of columns 4*tau + 1024*i in registers.  Eight values (4 rows x
+// 2 tokens) are reduced per warp, so every score is summed by the same tree
+// whatever T is: a token's route does not depend on the rest of the batch.
+constexpr int kRgRows = 4;
+constexpr int kRgThreads = 256;
+constexpr int kRgChunks = 8;  // float4 chunks per thread per row: H <= 8192
+
+template <bool XBF16>
+__device__ __forceinline__ float4 load_x4(const void* x, int64_t idx) {
+  if (XBF16) {
+    const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(x) + idx);
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  } else {
+    return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx);
+  }
+}
+
+// Single-CTA tail: top-k and bucketing of T <= 64 tokens (E <= 4096) from the
+// scores in ws.logits.  Writes ids, w, offsets, sorted (workspace and caller
+// copies) and the active-expert list.
+__device__ void route_tail_small(const RouteParams& p, char* smem) {
+  const int T = p.T, E = p.E, k = p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  unsigned long long* tmask = reinterpret_cast<unsigned long long*>(smem);  // [E] token bits
+  int* cnt = reinterpret_cast<int*>(tmask + E);                             // [E]
+  int* off = cnt + E;                                                        // [E+1]
+  int* s_ids = off + E + 1;                                                  // [T*k]
+  s_ids = reinterpret_cast<int*>((reinterpret_cast<uintptr_t>(s_ids) + 15) & ~(uintptr_t)15);
+  float2* rows = reinterpret_cast<float2*>(s_ids + kDecodeMaxT * kMaxK);     // [nwarps][E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) tmask[e] = 0ull;
+  __syncthreads();
+  for (int t = warp; t < T; t += nwarps) {
+    float2* row = rows + (size_t)warp * E;
+    for (int e = lane; e < E; e += 32) row[e] = __ldcg(&p.ws.logits[(size_t)t * E + e]);
+    __syncwarp();
+    int my_e;
+    float2 my_s;
+    warp_topk(row, E, k, my_e, my_s);
+    const float wt = warp_route_weight(my_s, k);
+    if (lane < k) {
+      p.ids[t * k + lane] = my_e;
+      p.w[t * k + lane] = wt;
+      s_ids[t * k + lane] = my_e;
+      atomicOr(&tmask[my_e], 1ull << t);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = __popcll(tmask[e]);
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0, nact = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? cnt[e] : 0;
+      int incl = c;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+        if (lane >= m) incl += o;
+      }
+      const unsigned act = __ballot_sync(0xFFFFFFFFu, c > 0);
+      if (e < E) {
+        off[e] = run + incl - c;
+        if (c > 0) p.ws.act_e[nact + __popc(act & ((1u << lane) - 1u))] = e;
+      }
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      nact += __popc(act);
+    }
+    if (lane == 0) {
+      off[E] = run;
+      p.ws.hdr->n_active = (uint32_t)nact;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    p.ws.offsets[e] = off[e];
+    if (p.offsets) p.offsets[e] = off[e];
+  }
+  // Stable scatter: the rank of token t in expert e's bucket is the number of
+  // tokens below t routed to e (a token selects an expert at most once).
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int e = s_ids[i];
+    const unsigned long long below = t == 0 ? 0ull : (tmask[e] & ((1ull << t) - 1ull));
+    const int pos = off[e] + __popcll(below);
+    p.ws.sorted[pos] = i;
+    if (p.sorted) p.sorted[pos] = i;
+  }
+}
+
+size_t route_tail_smem_bytes(int E) {
+  return (size_t)E * 8 + (size_t)E * 4 + (size_t)(E + 1) * 4 + (size_t)kDecodeMaxT * kMaxK * 4 + 16 +
+         (size_t)(kRgThreads / 32) * E * 8 + 64;
+}
+
+template <bool XBF16>
+__global__ void __launch_bounds__(kRgThreads) k_router_gemv(RouteParams p) {
+  extern __shared__ float4 dyn_smem4[];
+  __shared__ float2 red[kRgThreads / 32][8];
+  __shared__ int is_last;
+  const int H = p.H, E = p.E, T = p.T;
+  const int ncols4 = H / 4;
+  const int e0 = blockIdx.x * kRgRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  for (int tp = 0; tp < T; tp += 2) {
+    float4 xr[2][kRgChunks];
+#pragma unroll
+    for (int i = 0; i < kRgChunks; ++i) {
+      const int c4 = threadIdx.x + i * kRgThreads;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int t = tp + q;
+        xr[q][i] = (c4 < ncols4 && t < T) ? load_x4<XBF16>(p.x, (int64_t)t * H + (int64_t)c4 * 4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    // Each float4 chunk (4 products) is summed in fp32, then added into a
+    // double-float accumulator; the reductions below stay double-float.
+    float ah[8], al[8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) { ah[v] = 0.f; al[v] = 0.f; }
+#pragma unroll
+    for (int i = 0; i < kRgChunks; ++i) {
+      const int c4 = threadIdx.x + i * kRgThreads;
+      if (c4 < ncols4) {
+        float4 wv[kRgRows];
+#pragma unroll
+        for (int r = 0; r < kRgRows; ++r) {
+          const int e = e0 + r < E ? e0 + r : E - 1;
+          wv[r] = __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)e * H) + c4);
+        }
+#pragma unroll
+        for (int r = 0; r < kRgRows; ++r)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            float a = wv[r].x * xr[q][i].x;
+            a = fmaf(wv[r].y, xr[q][i].y, a);
+            a = fmaf(wv[r].z, xr[q][i].z, a);
+            a = fmaf(wv[r].w, xr[q][i].w, a);
+            df_add_f(ah[r * 2 + q], al[r * 2 + q], a);
+          }
+      }
+    }
+    float th, tl;
+    warp_transpose_reduce_df<8>(ah, al, th, tl);
+    if (lane < 8) red[warp][lane] = make_float2(th, tl);
+    __syncthreads();
+    if (threadIdx.x < 8) {
+      float sh = 0.f, sl = 0.f;
+      for (int w = 0; w < kRgThreads / 32; ++w) df_add(sh, sl, red[w][threadIdx.x].x, red[w][threadIdx.x].y, sh, sl);
+      const int r = threadIdx.x >> 1, q = threadIdx.x & 1;
+      const int e = e0 + r, t = tp + q;
+      if (e < E && t < T) {
+        if (p.br) df_add(sh, sl, p.br[e], 0.f, sh, sl);
+        p.ws.logits[(size_t)t * E + e] = make_float2(sh, sl);
+      }
+    }
+    __syncthreads();
+  }
+  // The last CTA to finish routes and buckets all tokens.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&p.ws.hdr->route_ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  route_tail_small(p, reinterpret_cast<char*>(dyn_smem4));
+  if (threadIdx.x == 0) p.ws.hdr->route_ticket = 0u;
+}
+
+bool route_decode_supported(int T, int H, int E, int k) {
+  return T <= kDecodeMaxT && H <= kRgChunks * 4 * kRgThreads && E <= 4096 && k <= kMaxK;
+}
+
+cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
+  const size_t smem = route_tail_smem_bytes(p.E);
+  const dim3 grid((p.E + kRgRows - 1) / kRgRows);
+  auto kern = p.x_bf16 ? k_router_gemv<true> : k_router_gemv<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kRgThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- prefill router GEMM --
+// s = x Wr^T (+ b) in fp32 on CUDA cores: 64x64 output tiles, 16-wide K steps,
+// 4x4 outputs per thread.  Also clears the per-expert token masks.
+constexpr int kGmTile = 64, kGmK = 16;
+
+template <bool XBF16>
+__global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
+  __shared__ float xs[kGmK][kGmTile + 4];
+  __shared__ float ws_[kGmK][kGmTile + 4];
+  const int T = p.T, H = p.H, E = p.E;
+  const int t0 = blockIdx.y * kGmTile, e0 = blockIdx.x * kGmTile;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  {
+    const size_t nmask = (size_t)E * ((T + 31) / 32);
+    const size_t gtid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t gsz = (size_t)gridDim.x * gridDim.y * blockDim.x;
+    for (size_t i = gtid; i < nmask; i += gsz) p.ws.mask[i] = 0u;
+  }
+  // Each 16-wide K step is summed in fp32 and added into a double-float
+  // accumulator (hi, lo).
+  float ah[4][4], al[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { ah[i][j] = 0.f; al[i][j] = 0.f; }
+  for (int kk = 0; kk < H; kk += kGmK) {
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const int idx = threadIdx.x + l * 256;
+      const int r = idx >> 4, c = idx & 15;
+      const int t = t0 + r, e = e0 + r;
+      float xv = 0.f, wv = 0.f;
+      if (t < T)
+        xv = XBF16 ? bf16_f32(reinterpret_cast<const uint16_t*>(p.x)[(size_t)t * H + kk + c])
+                   : reinterpret_cast<const float*>(p.x)[(size_t)t * H + kk + c];
+      if (e < E) wv = p.wr[(size_t)e * H + kk + c];
+      xs[c][r] = xv;
+      ws_[c][r] = wv;
+    }
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kGmK; ++c) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[c][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws_[c][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) df_add_f(ah[i][j], al[i][j], acc[i][j]);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) {
+        float sh, sl;
+        df_add(ah[i][j], al[i][j], p.br ? p.br[e] : 0.f, 0.f, sh, sl);
+        p.ws.logits[(size_t)t * E + e] = make_float2(sh, sl);
+      }
+    }
+  }
+}
+
+// One warp per token: top-k, softmax weights, and the token's bit in the mask
+// of each selected expert.
+__global__ void __launch_bounds__(256) k_topk(RouteParams p) {
+  extern __shared__ float4 dyn_smem4[];
+  float2* rows = reinterpret_cast<float2*>(dyn_smem4);
+  const int E = p.E, k = p.k, T = p.T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  float2* row = rows + (size_t)warp * E;
+  for (int e = lane; e < E; e += 32) row[e] = p.ws.logits[(size_t)t * E + e];
+  __syncwarp();
+  int my_e;
+  float2 my_s;
+  warp_topk(row, E, k, my_e, my_s);
+  const float wt = warp_route_weight(my_s, k);
+  if (lane < k) {
+    p.ids[(size_t)t * k + lane] = my_e;
+    p.w[(size_t)t * k + lane] = wt;
+    const int W = (T + 31) / 32;
+    atomicOr(&p.ws.mask[(size_t)my_e * W + (t >> 5)], 1u << (t & 31));
+  }
+}
+
+// Mask bits from caller-given ids (experts-only calls without a bucket layout).
+__global__ void k_mask_from_ids(BucketParams p) {
+  const int T = p.T, k = p.k, E = p.E;
+  const int W = (T + 31) / 32;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * k) return;
+  const int e = p.ids[i];
+  if (e < 0 || e >= E) {
+    set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+    return;
+  }
+  const int t = i / k;
+  atomicOr(&p.ws.mask[(size_t)e * W + (t >> 5)], 1u << (t & 31));
+}
+
+// One warp per expert: popcounts of its token-mask words, their exclusive
+// prefix (wprefix) and its count.  The last CTA to finish scans the counts
+// into offsets and builds the plan.
+__global__ void __launch_bounds__(256) k_bucket_count(BucketParams p) {
+  __shared__ int is_last;
+  const int E = p.E, T = p.T;
+  const int W = (T + 31) / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (e < E) {
+    int run = 0;
+    for (int base = 0; base < W; base += 32) {
+      const int wi = base + lane;
+      const int c = wi < W ? __popc(p.ws.mask[(size_t)e * W + wi]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+        if (lane >= m) incl += o;
+      }
+      if (wi < W) p.ws.wprefix[(size_t)e * W + wi] = run + incl - c;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) p.ws.offsets[e] = run;  // the count; scanned by the last CTA
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&p.ws.hdr->ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  plan_scan(p);
+  if (threadIdx.x == 0) p.ws.hdr->ticket = 0u;
+}
+
+// One thread per routed pair: its position in the expert's bucket.
+__global__ void k_bucket_scatter(BucketParams p) {
+  const int T = p.T, k = p.k;
+  const int W = (T + 31) / 32;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * k) return;
+  const int t = i / k;
+  const int e = p.ids[i];
+  if (e < 0 || e >= p.E) return;
+  const uint32_t word = p.ws.mask[(size_t)e * W + (t >> 5)];
+  const int pos = p.ws.offsets[e] + p.ws.wprefix[(size_t)e * W + (t >> 5)] + __popc(word & ((1u << (t & 31)) - 1u));
+  p.ws.sorted[pos] = i;
+  if (p.sorted_out) p.sorted_out[pos] = i;
+}
+
+// Plan from a caller-given offsets array: counts, then the same scan.
+// A layout that is not a partition of [0, T*k) (decreasing offsets, or
+// offsets outside that range) is flagged and no expert work is planned.
+__global__ void __launch_bounds__(1024) k_plan_from_offsets(BucketParams p, const int32_t* offsets_in) {
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = (offsets_in[0] != 0 || offsets_in[p.E] > p.T * p.k) ? 1 : 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    const int c = offsets_in[e + 1] - offsets_in[e];
+    if (c < 0) bad = 1;
+    p.ws.offsets[e] = c < 0 ? 0 : c;
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+      p.ws.hdr->n_active = 0u;
+    }
+    return;
+  }
+  __threadfence_block();
+  __syncthreads();
+  BucketParams q = p;
+  q.offsets_out = nullptr;
+  plan_scan(q);
+}
+
+cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s) {
+  const dim3 g1((p.E + kGmTile - 1) / kGmTile, (p.T + kGmTile - 1) / kGmTile);
+  if (p.x_bf16)
+    k_router_gemm<true><<<g1, 256, 0, s>>>(p);
+  else
+    k_router_gemm<false><<<g1, 256, 0, s>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem = (size_t)8 * p.E * 8;
+  err = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  k_topk<<<(p.T + 7) / 8, 256, smem, s>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  k_bucket_count<<<(p.E + 7) / 8, 256, 0, s>>>(b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  k_bucket_scatter<<<(p.T * p.k + 255) / 256, 256, 0, s>>>(b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bucket_from_ids(const BucketParams& b, cudaStream_t s) {
+  const size_t W = ((size_t)b.T + 31) / 32;
+  cudaError_t err = cudaMemsetAsync(b.ws.mask, 0, (size_t)b.E * W * 4, s);
+  if (err != cudaSuccess) return err;
+  k_mask_from_ids<<<(b.T * b.k + 255) / 256, 256, 0, s>>>(b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  k_bucket_count<<<(b.E + 7) / 8, 256, 0, s>>>(b);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  k_bucket_scatter<<<(b.T * b.k + 255) / 256, 256, 0, s>>>(b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_from_offsets(const BucketParams& b, const int32_t* offsets, cudaStream_t s) {
+  k_plan_from_offsets<<<1, 1024, 0, s>>>(b, offsets);
+  return cudaGetLastError();
+}
+
+int device_sm_count() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached = n;
+    else
+      cached = kNumSMs;
+  }
+  return cached;
+}
+
+}  // namespace moe
