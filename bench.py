@@ -1,0 +1,488 @@
+"""Benchmark of the routed MXFP4 MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|wide|prefill|long|decode_i1536|tiny]
+
+A step is one pass of the whole layer (moe_forward: router, top-k, bucketing,
+MXFP4 experts, combine) over one batch of the workload.  The default workload
+is 1-token decode (H=7168, 896 MXFP4 experts, top-16, I=1408).  Inputs are
+synthetic and seeded; all 896 experts are resident in HBM.  Prints ONE JSON
+line (rank 0).  For N > 1 (torchrun) every rank runs an independent replica
+of the workload on its own GPU (the layer has no exchange step here), the
+time is the max over ranks and `value` counts the tokens of all ranks.
+
+--impl reference times the fp64 CPU oracle (the reference arm) on the host
+cores, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s & weight GB/s (decode) / TFLOP/s (prefill) vs GB300 roofline"
+L2_FLUSH_BYTES = 256 << 20   # > 2x the 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ device --
+class Layer:
+    """The workload resident on one GPU, called through the C ABI."""
+
+    def __init__(self, wl_name: str, device: str):
+        import torch
+
+        import mxfp4_routed_expert_moe_gb300 as moe
+        import synth
+        self.torch, self.moe, self.synth = torch, moe, synth
+        self.wl = wl = synth.WORKLOADS[wl_name]
+        self.inp = inp = synth.make_inputs(wl)
+        self.device = device
+        self.table = moe.ExpertTable(wl.E, wl.H, wl.I, device)
+        offs, stride = synth.expert_blob_layout(wl)
+        assert (offs, stride) == moe.ExpertTable.blob_layout(wl.H, wl.I)
+        synth.fill_experts_device(inp, self.table.blob.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        if wl.x_dtype == "f32":
+            self.x_host = torch.from_numpy(inp.x).pin_memory()
+        else:
+            self.x_host = torch.from_numpy(inp.x.view("int16")).view(torch.bfloat16).pin_memory()
+        self.x = self.x_host.to(device)
+        self.wr = torch.from_numpy(inp.wr).to(device)
+        self.br = None if inp.br is None else torch.from_numpy(inp.br).to(device)
+        self.shared = None
+        if inp.shared is not None:
+            self.shared = tuple(torch.from_numpy(a.view("int16")).view(torch.bfloat16).to(device) for a in inp.shared)
+        self.shape = moe.shape(wl.T, wl.H, wl.E, wl.I, wl.k)
+        self.ws = torch.empty(moe.workspace_bytes(wl.T, wl.H, wl.E, wl.I, wl.k), dtype=torch.uint8, device=device)
+        self.out = torch.zeros((wl.T, wl.H), dtype=torch.float32, device=device)
+        self.out_host = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
+        self.ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device=device)
+        self.w = torch.empty((wl.T, wl.k), dtype=torch.float32, device=device)
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        torch.cuda.synchronize()
+
+    def step(self):
+        self.moe.forward(self.shape, self.x, self.wr, self.br, self.table.desc, self.shared, self.out, False,
+                         self.ws, ids_out=self.ids, w_out=self.w)
+
+    def flush_l2(self):
+        self.flush_buf.fill_(1.0)
+
+    @property
+    def decode_path(self) -> bool:
+        return self.wl.T <= self.moe.DECODE_MAX_T or self.wl.x_dtype == "f32"
+
+    def launches_per_step(self) -> int:
+        # decode: router(+top-k tail), gate/up, down, combine
+        # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, gate/up, down (+ shared)
+        if self.decode_path:
+            return 4
+        return 7 + (2 if self.shared is not None else 0)
+
+    def dominant_stage(self):
+        return self.moe.STAGE_GATEUP if self.decode_path else self.moe.STAGE_PF_GATEUP
+
+    def active_experts(self) -> int:
+        return len(set(self.ids.cpu().numpy().ravel().tolist()))
+
+    def algorithmic_bytes_step(self, n_active: int) -> int:
+        wl = self.wl
+        xb = wl.T * wl.H * (4 if wl.x_dtype == "f32" else 2)
+        b = n_active * wl.expert_bytes + wl.E * wl.H * 4 + xb + wl.T * wl.H * 4
+        if self.shared is not None:
+            b += 3 * wl.H * wl.I * 2
+        return b
+
+    def algorithmic_bytes_gateup(self, n_active: int) -> int:
+        wl = self.wl
+        xb = wl.T * wl.H * (4 if wl.x_dtype == "f32" else 2)
+        return n_active * 2 * (wl.I * wl.H // 2 + wl.I * wl.H // 32) + xb + wl.T * wl.k * wl.I * 4
+
+    def flops_step(self) -> int:
+        return self.wl.T * self.wl.flops_per_token
+
+
+def time_steps(layer, steps, warmup, use_graph):
+    """Device time of each of `steps` steps (ms), L2 flushed before each."""
+    torch = layer.torch
+    fn = layer.step
+    graph = None
+    if use_graph:
+        layer.step()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            layer.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.step()
+        fn = graph.replay
+    for _ in range(warmup):
+        layer.flush_l2()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        layer.flush_l2()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], graph
+
+
+def time_stage(layer, stage, reps):
+    """Mean duration (ms) of one stage's kernel, bracketed by events the
+    library records on the launching stream (profiling hook)."""
+    torch = layer.torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(); b.record()  # materialise the events
+    torch.cuda.synchronize()
+    times = []
+    layer.moe.profile_events(stage, a, b)
+    try:
+        for _ in range(reps):
+            layer.flush_l2()
+            layer.step()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+    finally:
+        layer.moe.profile_events(stage, None, None)
+    return statistics.mean(times)
+
+
+def time_e2e(layer, steps, warmup, graph):
+    """Same metric through the C ABI with host buffers: pinned H2D of the
+    step's activations, the layer, D2H of its output, all inside the timing."""
+    torch = layer.torch
+    fn = graph.replay if graph is not None else layer.step
+    for _ in range(warmup):
+        layer.flush_l2()
+        layer.x.copy_(layer.x_host, non_blocking=True)
+        fn()
+        layer.out_host.copy_(layer.out, non_blocking=True)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        layer.flush_l2()
+        a.record()
+        layer.x.copy_(layer.x_host, non_blocking=True)
+        fn()
+        layer.out_host.copy_(layer.out, non_blocking=True)
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def traffic_from_profiles(kernel_tag: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/*.md line
+    `traffic_bytes_per_launch: <n> source_sha: <sha>`), or None when the
+    kernel sources changed since."""
+    src = hashlib.sha256()
+    for f in ("common.cuh", "decode.cu", "prefill.cu", "tcgen05.cuh"):
+        p = os.path.join(ROOT, "mxfp4_routed_expert_moe_gb300", "csrc", f)
+        if os.path.exists(p):
+            src.update(open(p, "rb").read())
+    sha = src.hexdigest()[:16]
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None, sha
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        text = open(os.path.join(pdir, f)).read()
+        m = re.search(rf"traffic\[{re.escape(kernel_tag)}\]: bytes_per_launch=(\d+) source_sha=(\w+)", text)
+        if m and m.group(2) == sha:
+            return int(m.group(1)), sha
+    return None, sha
+
+
+# ------------------------------------------------------------------- oracle --
+def cpu_baseline(layer, seconds: float):
+    """The fp64 oracle on the host cores on a bounded sample of the workload:
+    whole tokens of the layer, repeated until `seconds` of CPU time elapsed.
+    Also returns the oracle-vs-GPU error on the sampled tokens."""
+    import numpy as np
+
+    import oracle
+    inp, wl = layer.inp, layer.wl
+    threads = oracle.default_threads()
+    tokens = []
+    t0 = time.perf_counter()
+    outs = []
+    i = 0
+    while True:
+        tok = (i * 7919) % wl.T
+        out, ids, w = oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array([tok]),
+                                        shared=inp.shared, nthreads=threads)
+        tokens.append(tok)
+        outs.append(out[0])
+        i += 1
+        if time.perf_counter() - t0 >= seconds or i >= 64:
+            break
+    # Exclude the on-demand host generation of expert weights from the timing:
+    # time the same sample again with every expert already materialised.
+    t0 = time.perf_counter()
+    for tok in tokens:
+        oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array([tok]), shared=inp.shared,
+                          nthreads=threads)
+    dt = time.perf_counter() - t0
+    got = layer.out.cpu().numpy().astype(np.float64)
+    ref = np.stack(outs)
+    err = got[tokens] - ref
+    rel = float(np.linalg.norm(err) / np.linalg.norm(ref))
+    return {"value": len(tokens) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(tokens)} token(s) of {wl.name} through the whole layer (fp64, {threads} threads)",
+            "seconds": round(dt, 3)}, {"tokens": len(tokens), "rel_l2_vs_oracle": rel}
+
+
+def reference_arm(args, rank, world):
+    """The fp64 oracle as the reference implementation, K timed steps."""
+    import numpy as np
+
+    import oracle
+    import synth
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl)
+    threads = oracle.default_threads()
+    toks = lambda i: np.array([(i * 7919) % wl.T])
+    # Materialise the experts of the sampled tokens first (input generation).
+    n_total = args.steps + args.warmup
+    t0 = time.perf_counter()
+    oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, toks(0), shared=inp.shared, nthreads=threads)
+    t_tok = time.perf_counter() - t0
+    budget = 150.0
+    # Per-step sample: one token through the layer if the run fits the budget,
+    # else the expert MLPs of a subset of one token's routed slots (the
+    # route is still computed every step).
+    slots = wl.k if n_total * t_tok <= budget else max(1, int(wl.k * budget / (n_total * t_tok)))
+    s = oracle.router_logits(inp.x[toks(0)], inp.wr, inp.br, threads)
+    ids0, _, _ = oracle.topk(s, wl.k)
+    for e in ids0[0]:
+        inp.expert(int(e))
+    x0 = inp.x_f32[toks(0)[0]].astype(np.float64)
+
+    def one_step(i):
+        if slots == wl.k:
+            oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, toks(0), shared=inp.shared,
+                              nthreads=threads)
+        else:
+            s = oracle.router_logits(inp.x[toks(0)], inp.wr, inp.br, threads)
+            ids, _, _ = oracle.topk(s, wl.k)
+            from concurrent.futures import ThreadPoolExecutor
+            with ThreadPoolExecutor(max_workers=slots) as ex:
+                list(ex.map(lambda j: oracle.expert_mlp(wl.H, wl.I, x0, inp.expert(int(ids[0, (i + j) % wl.k]))),
+                            range(slots)))
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_step(i)
+    dt = time.perf_counter() - t0
+    tokens_per_step = slots / wl.k
+    value = args.steps * tokens_per_step / dt
+    sample = (f"1 token of {wl.name} per step through the whole layer" if slots == wl.k else
+              f"per step: route + {slots} of the {wl.k} routed expert MLPs of 1 token of {wl.name}")
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": wl.name, "tokens_per_step": tokens_per_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- main --
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = f"cuda:{torch.cuda.current_device()}"
+    layer = Layer(args.workload, device)
+    wl = layer.wl
+
+    # Untimed correctness probe through the library's device status word.
+    layer.step()
+    torch.cuda.synchronize()
+    st = layer.moe.device_status(layer.ws)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({layer.moe.status_string(st)})")
+    n_active = layer.active_experts()
+
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    step_ms, graph = time_steps(layer, args.steps, max(args.warmup, 3), not args.no_graph)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.T / (ms / 1000.0)
+
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    stage = layer.dominant_stage()
+    st_ms = time_stage(layer, stage, reps=20)
+    e2e_ms = time_e2e(layer, max(20, min(args.steps, 200)), 3, graph)
+    nograph_ms = statistics.mean(time_steps(layer, 50, 3, False)[0]) if not args.no_graph else ms
+    if layer.decode_path:
+        gu_bytes = layer.algorithmic_bytes_gateup(n_active)
+        achieved = gu_bytes / (st_ms / 1000.0) / 1e9
+        traffic, sha = traffic_from_profiles("dec_gateup_" + wl.name)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "kernel": "k_dec_gateup (MXFP4 gate/up GEMV + SwiGLU)",
+                "bytes_per_launch": gu_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
+    else:
+        roof = None
+    step_bytes = layer.algorithmic_bytes_step(n_active)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if wl.x_dtype == "f32" else "bf16 activations, MXFP4 weights, fp32 accumulate",
+        "data": "synthetic (seeded; 896 experts resident in HBM)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "path": "decode" if layer.decode_path else "prefill", "cuda_graph": not args.no_graph,
+                   "l2": "flushed before every step (256 MiB write, outside the step timing)",
+                   "active_experts": n_active, "parallelism": f"replicas x{world}"},
+        "weight_gbps": step_bytes / (ms / 1000.0) / 1e9,
+        "step_roofline": {"bytes": step_bytes, "frac_hbm": step_bytes / (ms / 1000.0) / 1e9 / hbm,
+                          "tflops": layer.flops_step() / (ms / 1000.0) / 1e12},
+        "no_graph_ms_per_step": nograph_ms,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": {"value": world * wl.T / (e2e_ms / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": layer.x.numel() * layer.x.element_size(),
+                "d2h_bytes_per_step": layer.out.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": layer.launches_per_step() * args.steps,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        cb, parity = cpu_baseline(layer, args.cpu_seconds)
+        line["cpu_baseline"] = cb
+        line["parity_on_cpu_sample"] = parity
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -51,8 +51,11 @@
  *     (work is enqueued on `stream`, so buffers must stay valid until it has
  *     run).  `shape` and `shared` point to HOST structs; `experts` points to a
  *     DEVICE array of E moe_expert descriptors.
- *   - Alignment: x, q tensors, out, ws: 16 bytes; everything else: its
- *     element size.  Misalignment is MOE_ERR_INVALID_ARG.
+ *   - Alignment: x, out, shared-expert tensors: 16 bytes; ws: 256 bytes;
+ *     every expert tensor (q and s): 16 bytes; everything else: its element
+ *     size.  Host-visible misalignment is MOE_ERR_INVALID_ARG; an expert
+ *     descriptor (device memory) with a null or misaligned tensor is detected
+ *     on the device (MOE_ERR_DEVICE_CHECK) and that expert is not read.
  *   - Asynchrony: calls enqueue kernels on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and return; there is no host synchronisation
  *     except in moe_device_status().  The calls make no CUDA allocation.
@@ -169,6 +172,27 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
  * began with this workspace).  Returns MOE_ERR_CUDA if the synchronisation or
  * the copy fails. */
 int moe_device_status(const void* ws, void* stream, int* status_out);
+
+/* Kernel stages, for the profiling hook below. */
+typedef enum {
+  MOE_STAGE_ROUTE = 1,        /* router scores (+ fused top-k/bucketing on the decode path) */
+  MOE_STAGE_GATEUP = 2,       /* decode gate/up MXFP4 GEMV + SwiGLU */
+  MOE_STAGE_DOWN = 3,         /* decode down MXFP4 GEMV */
+  MOE_STAGE_COMBINE = 4,      /* decode slot-ordered combine */
+  MOE_STAGE_PF_GATEUP = 5,    /* prefill grouped gate/up GEMM + SwiGLU */
+  MOE_STAGE_PF_DOWN = 6,      /* prefill grouped down GEMM + combine */
+  MOE_STAGE_COUNT = 7
+} moe_stage;
+
+/* Profiling hook, for benchmarks (process-wide, not thread-safe): while set,
+ * every call records the CUDA event `before` (a cudaEvent_t) on its stream
+ * right before it launches the kernel of `stage`, and `after` right after.
+ * Recording events between kernels removes the programmatic-dependent-launch
+ * overlap at that point, so a hooked call is slightly slower than an unhooked
+ * one.  Pass NULL events to clear.  Returns MOE_ERR_INVALID_ARG for an unknown
+ * stage.  [Deltafin's custom compiled runtime, "Verification boundaries":
+ * benchmark events that refuse oracle-mismatched runs.] */
+int moe_profile_events(int stage, void* before, void* after);
 
 #ifdef __cplusplus
 }

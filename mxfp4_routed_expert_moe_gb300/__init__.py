@@ -34,7 +34,9 @@ DECODE_MAX_T = 64
 
 # Every symbol the header declares (checked by the tests against the .so).
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_route", "moe_mxfp4_experts",
-           "moe_forward", "moe_device_status")
+           "moe_forward", "moe_device_status", "moe_profile_events")
+
+STAGE_ROUTE, STAGE_GATEUP, STAGE_DOWN, STAGE_COMBINE, STAGE_PF_GATEUP, STAGE_PF_DOWN = 1, 2, 3, 4, 5, 6
 
 
 class MoeError(RuntimeError):
@@ -76,6 +78,7 @@ def lib():
             L.moe_mxfp4_experts.argtypes = [P(Shape), vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp]
             L.moe_forward.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp, i32, vp, sz, vp]
             L.moe_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
+            L.moe_profile_events.argtypes = [i32, vp, vp]
             _LIB = L
     return _LIB
 
@@ -156,6 +159,14 @@ def forward(shp: Shape, x, w_router, b_router, experts, shared, out, accumulate,
                            _ptr(experts), sh, _ptr(out), int(bool(accumulate)), _ptr(ids_out), _ptr(w_out),
                            int(path), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "moe_forward")
+
+
+def profile_events(stage: int, before=None, after=None) -> None:
+    """Record torch.cuda.Event `before`/`after` around the kernel of `stage`
+    in subsequent calls (None clears)."""
+    b = None if before is None else before.cuda_event
+    a = None if after is None else after.cuda_event
+    _check(lib().moe_profile_events(int(stage), b, a), "moe_profile_events")
 
 
 def device_status(ws, stream=None) -> int:

@@ -7,6 +7,10 @@
 
 using namespace moe;
 
+namespace moe {
+ProfHook g_prof = {};
+}
+
 namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -208,6 +212,13 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
     return st;
   const ExpertParams p = expert_params(shape, x, x_dtype, experts, ids, w, L.offsets, L.sorted, out, accumulate, shared, L);
   return run_experts(p, rpath, s);
+}
+
+int moe_profile_events(int stage, void* before, void* after) {
+  if (stage < 1 || stage >= MOE_STAGE_COUNT) return MOE_ERR_INVALID_ARG;
+  g_prof.before[stage] = (cudaEvent_t)before;
+  g_prof.after[stage] = (cudaEvent_t)after;
+  return MOE_OK;
 }
 
 int moe_device_status(const void* ws, void* stream, int* status_out) {

@@ -91,6 +91,14 @@ __device__ __forceinline__ void set_status(WsHeader* hdr, uint32_t st) {
   atomicCAS(&hdr->status, 0u, st);
 }
 
+// Every tensor pointer of an expert descriptor non-null and 16-byte aligned
+// (bulk copies and 128-bit loads require it).
+__device__ __forceinline__ bool expert_ptrs_ok(const moe_expert& ex) {
+  const uintptr_t a = (uintptr_t)ex.gate.q | (uintptr_t)ex.gate.s | (uintptr_t)ex.up.q | (uintptr_t)ex.up.s |
+                      (uintptr_t)ex.down.q | (uintptr_t)ex.down.s;
+  return (a & 15u) == 0 && ex.gate.q && ex.gate.s && ex.up.q && ex.up.s && ex.down.q && ex.down.s;
+}
+
 // E8M0 scale byte -> fp32 2^(s-127); s = 0 gives the subnormal 2^-127, s = 255 NaN.
 __device__ __forceinline__ float e8m0_f32(uint32_t s) {
   uint32_t bits = s == 0u ? 0x00400000u : (s << 23);

@@ -26,6 +26,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 int device_sm_count();
 
+// Raise a kernel's dynamic shared memory limit to at least `bytes` (once per
+// kernel and size; later calls are a table lookup).
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes);
+// Resident CTAs per SM of a kernel for a block size and dynamic smem (>= 1),
+// memoised.
+cudaError_t cached_occupancy(const void* kernel, int threads, size_t smem, int* out);
+
+// Profiling hook state (see moe_profile_events in the header).
+struct ProfHook {
+  cudaEvent_t before[MOE_STAGE_COUNT];
+  cudaEvent_t after[MOE_STAGE_COUNT];
+};
+extern ProfHook g_prof;
+inline void prof_before(int stage, cudaStream_t s) {
+  if (g_prof.before[stage]) cudaEventRecord(g_prof.before[stage], s);
+}
+inline void prof_after(int stage, cudaStream_t s) {
+  if (g_prof.after[stage]) cudaEventRecord(g_prof.after[stage], s);
+}
+
 // route.cu
 bool route_decode_supported(int T, int H, int E, int k);
 cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s);

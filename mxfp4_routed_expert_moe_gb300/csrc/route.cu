@@ -316,9 +316,11 @@ cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
   const size_t smem = route_tail_smem_bytes(p.E);
   const dim3 grid((p.E + kRgRows - 1) / kRgRows);
   auto kern = p.x_bf16 ? k_router_gemv<true> : k_router_gemv<false>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = ensure_smem_attr((const void*)kern, smem);
   if (err != cudaSuccess) return err;
+  prof_before(MOE_STAGE_ROUTE, s);
   kern<<<grid, kRgThreads, smem, s>>>(p);
+  prof_after(MOE_STAGE_ROUTE, s);
   return cudaGetLastError();
 }
 
@@ -519,14 +521,16 @@ __global__ void __launch_bounds__(1024) k_plan_from_offsets(BucketParams p, cons
 
 cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s) {
   const dim3 g1((p.E + kGmTile - 1) / kGmTile, (p.T + kGmTile - 1) / kGmTile);
+  prof_before(MOE_STAGE_ROUTE, s);
   if (p.x_bf16)
     k_router_gemm<true><<<g1, 256, 0, s>>>(p);
   else
     k_router_gemm<false><<<g1, 256, 0, s>>>(p);
+  prof_after(MOE_STAGE_ROUTE, s);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = (size_t)8 * p.E * 8;
-  err = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  err = ensure_smem_attr((const void*)k_topk, smem);
   if (err != cudaSuccess) return err;
   k_topk<<<(p.T + 7) / 8, 256, smem, s>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -551,6 +555,36 @@ cudaError_t launch_bucket_from_ids(const BucketParams& b, cudaStream_t s) {
 cudaError_t launch_plan_from_offsets(const BucketParams& b, const int32_t* offsets, cudaStream_t s) {
   k_plan_from_offsets<<<1, 1024, 0, s>>>(b, offsets);
   return cudaGetLastError();
+}
+
+namespace {
+struct KeyVal { const void* k; int a; size_t b; int v; };
+KeyVal g_smem_attr[64];
+KeyVal g_occ[64];
+int g_n_smem = 0, g_n_occ = 0;
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
+  for (int i = 0; i < g_n_smem; ++i)
+    if (g_smem_attr[i].k == kernel && g_smem_attr[i].b >= bytes) return cudaSuccess;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (err != cudaSuccess) return err;
+  for (int i = 0; i < g_n_smem; ++i)
+    if (g_smem_attr[i].k == kernel) { g_smem_attr[i].b = bytes; return cudaSuccess; }
+  if (g_n_smem < 64) g_smem_attr[g_n_smem++] = {kernel, 0, bytes, 0};
+  return cudaSuccess;
+}
+
+cudaError_t cached_occupancy(const void* kernel, int threads, size_t smem, int* out) {
+  for (int i = 0; i < g_n_occ; ++i)
+    if (g_occ[i].k == kernel && g_occ[i].a == threads && g_occ[i].b == smem) { *out = g_occ[i].v; return cudaSuccess; }
+  int occ = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
+  if (err != cudaSuccess) return err;
+  if (occ < 1) occ = 1;
+  if (g_n_occ < 64) g_occ[g_n_occ++] = {kernel, threads, smem, occ};
+  *out = occ;
+  return cudaSuccess;
 }
 
 int device_sm_count() {

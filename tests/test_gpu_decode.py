@@ -217,3 +217,25 @@ def test_device_generator_matches_host_generator():
         ex = inp.expert(e)
         for j, n in enumerate(names):
             assert np.array_equal(table.tensor(e, j).cpu().numpy(), ex[n]), (e, n)
+
+
+def test_misaligned_expert_descriptor_is_flagged_not_read():
+    """An expert whose descriptor holds a misaligned tensor pointer is flagged
+    (MOE_ERR_DEVICE_CHECK) and never dereferenced; the next clean call is ok."""
+    t = torch()
+    wl = _small_workload("misal", 4, 256, 8, 2, 128)
+    inp = synth.make_inputs(wl, seed=4)
+    inp.br = np.zeros(wl.E, dtype=np.float32)
+    inp.br[3] = 100.0
+    L = DeviceLayer(inp)
+    good = L.table.desc.clone()
+    bad = good.clone()
+    bad[3, 0] += 8  # gate.q of expert 3, no longer 16-byte aligned
+    L.table.desc.copy_(bad)
+    out, ids, w = L.forward(path=1)
+    assert L.status() == L.moe.MOE_ERR_DEVICE_CHECK
+    assert np.all(ids.cpu().numpy()[:, 0] == 3)
+    L.table.desc.copy_(good)
+    out, ids, w = L.forward(path=1)
+    assert L.status() == 0
+    check_out(out.cpu().numpy(), oracle_out(inp, np.arange(wl.T)), "after misaligned")
