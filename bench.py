@@ -166,10 +166,10 @@ class Layer:
         return self.wl.T <= self.moe.DECODE_MAX_T or self.wl.x_dtype == "f32"
 
     def launches_per_step(self) -> int:
-        # decode: router(+top-k tail), gate/up, down, combine
+        # decode: router(+top-k tail), gate/up, down(+combine)
         # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, gate/up, down (+ shared)
         if self.decode_path:
-            return 4
+            return 3  # router (+ fused top-k/bucketing), gate/up, down (+ fused combine)
         return 7 + (2 if self.shared is not None else 0)
 
     def dominant_stage(self):
@@ -247,6 +247,48 @@ def time_stage(layer, stage, reps):
     return statistics.mean(times)
 
 
+def stage_breakdown(layer, reps=20):
+    """Mean device time (ms) of each kernel stage of one step (profiling
+    hook), and of an experts-only call given the route."""
+    moe, torch = layer.moe, layer.torch
+    out = {}
+    stages = ([("router", moe.STAGE_ROUTE), ("gate_up", moe.STAGE_GATEUP), ("down", moe.STAGE_DOWN)]
+              if layer.decode_path else
+              [("router", moe.STAGE_ROUTE), ("gate_up", moe.STAGE_PF_GATEUP), ("down", moe.STAGE_PF_DOWN)])
+    for name, st in stages:
+        try:
+            out[name] = time_stage(layer, st, reps)
+        except Exception as exc:  # stage not launched on this path
+            out[name] = None
+    wl = layer.wl
+    ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device=layer.device)
+    w = torch.empty((wl.T, wl.k), dtype=torch.float32, device=layer.device)
+    off = torch.empty(wl.E + 1, dtype=torch.int32, device=layer.device)
+    srt = torch.empty(wl.T * wl.k, dtype=torch.int32, device=layer.device)
+    moe.route(layer.shape, layer.x, layer.wr, layer.br, ids, w, off, srt, layer.ws)
+    o2 = torch.zeros_like(layer.out)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t = []
+    for _ in range(reps):
+        layer.flush_l2()
+        a.record()
+        moe.mxfp4_experts(layer.shape, layer.x, layer.table.desc, ids, w, off, srt, o2, False, layer.ws)
+        b.record()
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b))
+    out["experts_call_given_route"] = statistics.mean(t)
+    t = []
+    for _ in range(reps):
+        layer.flush_l2()
+        a.record()
+        moe.route(layer.shape, layer.x, layer.wr, layer.br, ids, w, off, srt, layer.ws)
+        b.record()
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b))
+    out["route_call"] = statistics.mean(t)
+    return out
+
+
 def time_e2e(layer, steps, warmup, graph):
     """Same metric through the C ABI with host buffers: pinned H2D of the
     step's activations, the layer, D2H of its output, all inside the timing."""
@@ -270,16 +312,27 @@ def time_e2e(layer, steps, warmup, graph):
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
-def traffic_from_profiles(kernel_tag: str):
-    """DRAM bytes per launch recorded by an ncu capture (profiles/*.md line
-    `traffic_bytes_per_launch: <n> source_sha: <sha>`), or None when the
-    kernel sources changed since."""
+KERNEL_SOURCES = {
+    "dec_gateup": ("common.cuh", "async.cuh", "route_small.cuh", "decode.cu"),
+    "pf_gateup": ("common.cuh", "async.cuh", "tcgen05.cuh", "prefill.cu"),
+}
+
+
+def source_sha(kernel: str) -> str:
     src = hashlib.sha256()
-    for f in ("common.cuh", "decode.cu", "prefill.cu", "tcgen05.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         p = os.path.join(ROOT, "mxfp4_routed_expert_moe_gb300", "csrc", f)
         if os.path.exists(p):
             src.update(open(p, "rb").read())
-    sha = src.hexdigest()[:16]
+    return src.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture (a profiles/*.md line
+    `traffic[<kernel>:<workload>]: bytes_per_launch=<n> source_sha=<sha>`), or
+    None when the kernel's sources changed since the capture."""
+    sha = source_sha(kernel)
+    tag = f"{kernel}:{workload}"
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None, sha
@@ -287,7 +340,7 @@ def traffic_from_profiles(kernel_tag: str):
         if not f.endswith(".md"):
             continue
         text = open(os.path.join(pdir, f)).read()
-        m = re.search(rf"traffic\[{re.escape(kernel_tag)}\]: bytes_per_launch=(\d+) source_sha=(\w+)", text)
+        m = re.search(rf"traffic\[{re.escape(tag)}\]: bytes_per_launch=(\d+) source_sha=(\w+)", text)
         if m and m.group(2) == sha:
             return int(m.group(1)), sha
     return None, sha
@@ -442,11 +495,12 @@ def main():
     stage = layer.dominant_stage()
     st_ms = time_stage(layer, stage, reps=20)
     e2e_ms = time_e2e(layer, max(20, min(args.steps, 200)), 3, graph)
+    breakdown = stage_breakdown(layer)
     nograph_ms = statistics.mean(time_steps(layer, 50, 3, False)[0]) if not args.no_graph else ms
     if layer.decode_path:
         gu_bytes = layer.algorithmic_bytes_gateup(n_active)
         achieved = gu_bytes / (st_ms / 1000.0) / 1e9
-        traffic, sha = traffic_from_profiles("dec_gateup_" + wl.name)
+        traffic, sha = traffic_from_profiles("dec_gateup", wl.name)
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic, "kernel": "k_dec_gateup (MXFP4 gate/up GEMV + SwiGLU)",
                 "bytes_per_launch": gu_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
@@ -466,6 +520,7 @@ def main():
         "step_roofline": {"bytes": step_bytes, "frac_hbm": step_bytes / (ms / 1000.0) / 1e9 / hbm,
                           "tflops": layer.flops_step() / (ms / 1000.0) / 1e12},
         "no_graph_ms_per_step": nograph_ms,
+        "stage_ms": breakdown,
         "roofline": roof,
         "clocks": clk,
         "e2e": {"value": world * wl.T / (e2e_ms / 1000.0), "unit": "tokens/s",

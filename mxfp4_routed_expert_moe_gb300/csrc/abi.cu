@@ -67,6 +67,23 @@ BucketParams bucket_params(const moe_shape* s, const int32_t* ids, int32_t* offs
   return b;
 }
 
+RouteParams route_params(const moe_shape* s, const void* x, int x_dtype, const float* wr, const float* br,
+                         int32_t* ids, float* w, int32_t* offsets, int32_t* sorted, const Ws& ws) {
+  RouteParams p;
+  p.T = s->T; p.H = s->H; p.E = s->E; p.k = s->k;
+  p.x = x;
+  p.x_bf16 = x_dtype == MOE_DT_BF16;
+  p.wr = wr;
+  p.br = br;
+  p.ids = ids;
+  p.w = w;
+  p.offsets = offsets;
+  p.sorted = sorted;
+  p.want_buckets = 1;
+  p.ws = ws;
+  return p;
+}
+
 int do_route(const moe_shape* s, const void* x, int x_dtype, const float* wr, const float* br, int32_t* ids, float* w,
              int32_t* offsets, int32_t* sorted, const Ws& ws, bool want_decode_route, cudaStream_t st) {
   RouteParams p;
@@ -208,9 +225,12 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
   int32_t* ids = ids_out ? ids_out : L.ids;
   float* w = w_out ? w_out : L.w;
   if ((st = cuda_status(cudaMemsetAsync(L.hdr, 0, sizeof(WsHeader), s))) != MOE_OK) return st;
-  if ((st = do_route(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L, rpath == MOE_PATH_DECODE, s)) != MOE_OK)
-    return st;
   const ExpertParams p = expert_params(shape, x, x_dtype, experts, ids, w, L.offsets, L.sorted, out, accumulate, shared, L);
+  if (rpath == MOE_PATH_DECODE) {
+    const RouteParams rp = route_params(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L);
+    return cuda_status(launch_decode_forward(rp, bucket_params(shape, ids, nullptr, nullptr, L), p, s));
+  }
+  if ((st = do_route(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L, false, s)) != MOE_OK) return st;
   return run_experts(p, rpath, s);
 }
 

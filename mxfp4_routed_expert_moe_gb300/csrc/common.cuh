@@ -265,6 +265,8 @@ struct ExpertParams {
   int accumulate;
   const moe_dense_bf16* shared_dev;  // unused on device; shared pointers below
   const uint16_t *sh_gate, *sh_up, *sh_down;
+  int fused_route;       // decode: the gate/up kernel routes (from ws.logits) first
+  RouteParams rp;        // the route to compute when fused_route
   Ws ws;
 };
 

@@ -19,6 +19,7 @@
 
 #include "async.cuh"
 #include "kernels.h"
+#include "route_small.cuh"
 
 namespace moe {
 
@@ -278,14 +279,22 @@ __global__ void k_dec_combine(ExpertParams p) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / H4), c4 = (int)(i % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const float wj = p.w[t * k + j];
-      const float4 y = reinterpret_cast<const float4*>(p.ws.y + (size_t)(t * k + j) * H)[c4];
-      acc.x = fmaf(wj, y.x, acc.x);
-      acc.y = fmaf(wj, y.y, acc.y);
-      acc.z = fmaf(wj, y.z, acc.z);
-      acc.w = fmaf(wj, y.w, acc.w);
-    }
+    float wj[kMaxK];
+    float4 y[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) {
+        wj[j] = p.w[t * k + j];
+        y[j] = reinterpret_cast<const float4*>(p.ws.y + (size_t)(t * k + j) * H)[c4];
+      }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) {
+        acc.x = fmaf(wj[j], y[j].x, acc.x);
+        acc.y = fmaf(wj[j], y[j].y, acc.y);
+        acc.z = fmaf(wj[j], y[j].z, acc.z);
+        acc.w = fmaf(wj[j], y[j].w, acc.w);
+      }
     float4* o = reinterpret_cast<float4*>(p.out + (size_t)t * H) + c4;
     if (p.accumulate) {
       const float4 r = *o;
@@ -332,26 +341,105 @@ static cudaError_t launch_decode_ldg(const ExpertParams& p, cudaStream_t s) {
 }
 
 // ===================================================== bulk-copy staged path --
-// A producer warp streams each work item's weight rows (contiguous ranges of
-// nibbles and scales) into a ring of shared-memory stages with the bulk-copy
-// engine; consumer warps dequantize from shared memory.  The ring keeps
-// ~100 KB per SM in flight independently of the consumers' registers.
-constexpr int kGuGroups = 2;       // consumer row groups (one block column per thread each)
-constexpr int kGuGroupVals = 8;    // values reduced per warp: 2 matrices x (R/2) rows x NT
+// Per CTA (one per SM), three roles:
+//   * a producer thread streams each work item's weight rows (contiguous
+//     ranges of nibbles and scales) into a ring of shared-memory stages with
+//     the bulk-copy engine, keeping ~100 KB per SM in flight;
+//   * consumer warps dequantize from shared memory and reduce each row's
+//     partial sums inside the warp (transpose-reduce, fixed tree);
+//   * a reducer warp adds the warps' partials in a fixed order and writes the
+//     results, fed through two mbarrier-guarded slots, so the consumers never
+//     wait on a CTA-wide barrier.
+// Bucket metadata (active experts, their bucket offsets and the routed pairs)
+// is read once per CTA into shared memory.
 constexpr int kMaxStages = 8;
+constexpr int kMaxPairs = kDecodeMaxT * kMaxK;  // routed pairs of a decode batch
 
-struct RingSmem {
+struct Ring {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t red_full[2];
+  uint64_t red_empty[2];
   int item[kMaxStages];
   int abort_flag;
 };
 
-// Producer side of the ring, run by one thread.  `issue(item, stage_ptr, bar)`
-// starts the copies of one item; returns false if the ring was aborted.
+// Bucket metadata in shared memory: per active expert its id, bucket offset,
+// size and the NP tensor pointers the kernel streams (read and checked once
+// per CTA); and every routed pair (sorted by expert).
+struct Plan {
+  int U;
+  int* ue;
+  int* ub0;
+  int* un;
+  int* pairs;
+  const uint8_t** ptrs;  // [umax][NP], null for an expert with a bad descriptor
+};
+
+__host__ __device__ inline size_t plan_smem_bytes(int E, int npairs, int np) {
+  const int umax = E < npairs ? E : npairs;
+  return (size_t)(3 * umax + npairs) * 4 + 16 + (size_t)umax * np * 8;
+}
+
+__device__ Plan plan_carve(const ExpertParams& p, uint8_t* buf, int np) {
+  Plan pl;
+  const int npairs = p.T * p.k;
+  const int umax = p.E < npairs ? p.E : npairs;
+  pl.U = 0;
+  pl.ue = reinterpret_cast<int*>(buf);
+  pl.ub0 = pl.ue + umax;
+  pl.un = pl.ub0 + umax;
+  pl.pairs = pl.un + umax;
+  pl.ptrs = reinterpret_cast<const uint8_t**>((reinterpret_cast<uintptr_t>(pl.pairs + npairs) + 15) & ~(uintptr_t)15);
+  return pl;
+}
+
+// Plan from the published route (workspace / caller layout).
+__device__ void load_plan(const ExpertParams& p, Plan& pl) {
+  pl.U = (int)p.ws.hdr->n_active;
+  const int npairs = p.T * p.k;
+  for (int u = threadIdx.x; u < pl.U; u += blockDim.x) {
+    const int e = p.ws.act_e[u];
+    const int b0 = p.offsets[e];
+    pl.ue[u] = e;
+    pl.ub0[u] = b0;
+    pl.un[u] = p.offsets[e + 1] - b0;
+  }
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+    int v = p.sorted[i];
+    if (v < 0 || v >= npairs) {
+      set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+      v = -1;
+    }
+    pl.pairs[i] = v;
+  }
+}
+
+// Cache the tensor pointers of the active experts (after ue is known).
+// which: 0 = gate/up (gate.q, up.q, gate.s, up.s), 1 = down (down.q, down.s).
+__device__ void plan_cache_ptrs(const ExpertParams& p, Plan& pl, int which) {
+  for (int u = threadIdx.x; u < pl.U; u += blockDim.x) {
+    const moe_expert ex = p.experts[pl.ue[u]];
+    const bool ok = expert_ptrs_ok(ex);
+    if (!ok) set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+    if (which == 0) {
+      pl.ptrs[u * 4 + 0] = ok ? ex.gate.q : nullptr;
+      pl.ptrs[u * 4 + 1] = ok ? ex.up.q : nullptr;
+      pl.ptrs[u * 4 + 2] = ok ? ex.gate.s : nullptr;
+      pl.ptrs[u * 4 + 3] = ok ? ex.up.s : nullptr;
+    } else {
+      pl.ptrs[u * 2 + 0] = ok ? ex.down.q : nullptr;
+      pl.ptrs[u * 2 + 1] = ok ? ex.down.s : nullptr;
+    }
+  }
+}
+
+// Producer loop (one thread).  issue(item, stage, bar) starts one item's
+// copies.  On a timed-out wait it records MOE_ERR_TIMEOUT, tells the
+// consumers and drains its copies in flight before returning.
 template <typename NextItem, typename Issue>
-__device__ void ring_produce(RingSmem& rs, uint8_t* data, int stages, uint32_t stage_bytes, WsHeader* hdr,
-                            NextItem next_item, Issue issue) {
+__device__ void ring_produce(Ring& rs, uint8_t* data, int stages, uint32_t stage_bytes, WsHeader* hdr,
+                             NextItem next_item, Issue issue) {
   int issued_use[kMaxStages];
   for (int i = 0; i < kMaxStages; ++i) issued_use[i] = -1;
   bool ok = true;
@@ -361,7 +449,10 @@ __device__ void ring_produce(RingSmem& rs, uint8_t* data, int stages, uint32_t s
       ok = false;
       break;
     }
-    if (*(volatile int*)&rs.abort_flag) { ok = false; break; }
+    if (*(volatile int*)&rs.abort_flag) {
+      ok = false;
+      break;
+    }
     const int item = next_item();
     rs.item[s] = item;
     if (item < 0) {
@@ -374,77 +465,197 @@ __device__ void ring_produce(RingSmem& rs, uint8_t* data, int stages, uint32_t s
   if (!ok) {
     set_status(hdr, MOE_ERR_TIMEOUT);
     rs.abort_flag = 1;
-    // Drain: the CTA must not exit while copies into its shared memory are in
-    // flight.  Each wait is bounded.
     for (int s = 0; s < stages; ++s)
       if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
   }
 }
 
-// Gate/up + SwiGLU.  Item = (active expert u, tile of R = 8/NT rows); consumer
-// group c (threads [c*ncw*32, (c+1)*ncw*32)) handles local rows c, c+2, ...
+// h between the staged gate/up and down kernels is stored block-interleaved:
+// within each group of 4 blocks (128 values) the 16-byte chunk c of block
+// b sits at (c * 4 + b % 4) * 16 bytes, so the four blocks a warp of the down
+// kernel needs are read as 64 contiguous bytes per chunk (no bank conflict).
+// Requires I % 128 == 0.
+__device__ __forceinline__ size_t h_swz(int row) {
+  const int b = row >> 5, j = row & 31;
+  return (size_t)(b >> 2) * 128 + (size_t)(j >> 2) * 16 + (size_t)(b & 3) * 4 + (size_t)(j & 3);
+}
+
+// ---------------------------------------------------------- gate/up + SwiGLU --
+// Item = (active expert u, tile of R = 8/NT rows of gate and of up).  Consumer
+// group c (ncw warps, one block column per thread) handles local rows c, c+2..
+// With bf16 activations each token is carried in f16 scaled by 2^sigma_t
+// (largest magnitude in [2^12, 2^13)): an E2M1 weight times such a value has
+// at most 10 significant bits, so the f16 product is exact and the sums run in
+// fp32 (mixed f16 + f32 adds); 2^-sigma_t is applied to the final sums.
+constexpr int kGuGroups = 2;
+constexpr int kGuTmaVals = 8;  // per warp and pass: 2 matrices x (R/2) rows x NT
+constexpr int kGuRowsNT = 8;   // rows per item x NT (R = 8 / NT)
+
+struct GuRedMeta {
+  int r0;
+  int ent[2];
+  float inv[2];
+};
+
+// One MX block dotted with NT tokens held as scaled f16 pairs: acc[n] += sum.
+template <int NT>
+__device__ __forceinline__ void mx_block_dot_f16(const uint4 q, uint32_t s, const uint32_t (&xh)[NT][16],
+                                                 float (&acc)[NT]) {
+  // Four accumulator chains per token (even/odd element x even/odd word).
+  float pa[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) pa[n][c] = 0.f;
+  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t w2 = e2m1x2_f16x2(words[wd], b);
+      const int c0 = (wd & 1) * 2;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        uint32_t pr;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(pr) : "r"(w2), "r"(xh[n][wd * 4 + b]));
+        asm("{\n .reg .f16 pl, ph;\n mov.b32 {pl, ph}, %2;\n add.rn.f32.f16 %0, pl, %0;\n add.rn.f32.f16 %1, ph, %1;\n}"
+            : "+f"(pa[n][c0]), "+f"(pa[n][c0 + 1])
+            : "r"(pr));
+      }
+    }
+  }
+  const float sc = e8m0_f32(s);
+#pragma unroll
+  for (int n = 0; n < NT; ++n) acc[n] = fmaf((pa[n][0] + pa[n][1]) + (pa[n][2] + pa[n][3]), sc, acc[n]);
+}
+
 template <int NT, bool XBF16>
-__global__ void __launch_bounds__(544, 1) k_dec_gateup_tma(ExpertParams p, int stages, uint32_t stage_bytes) {
-  constexpr int R = 8 / NT;
-  constexpr int RG = R / kGuGroups;  // rows per group
+__global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int stages, uint32_t stage_bytes) {
+  constexpr int R = kGuRowsNT / NT;
+  constexpr int RG = R / kGuGroups;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ RingSmem rs;
-  __shared__ float red[16][kGuGroupVals];
+  __shared__ Ring rs;
+  __shared__ float red[2][16][kGuTmaVals];
+  __shared__ GuRedMeta rmeta[2];
+  __shared__ float gmax[kGuGroups][8];
   const int H = p.H, I = p.I, k = p.k;
   const int nbH = H / 32;
-  const int ncw = (nbH + 31) / 32;           // consumer warps per group
-  const int ncons = kGuGroups * ncw * 32;    // consumer threads
+  const int ncw = (nbH + 31) / 32;
+  const int ncons_w = kGuGroups * ncw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t qrow = (size_t)H / 2;
   const uint32_t qbytes = (uint32_t)(R * qrow), sbytes = (uint32_t)(R * nbH);
+  uint8_t* ring_data = smem;
+  const size_t ring_bytes = (size_t)stages * stage_bytes;
+  const size_t scratch_bytes = p.fused_route ? route_small_scratch_bytes(p.E, blockDim.x / 32, p.T) : 0;
+  Plan pl = plan_carve(p, smem + (ring_bytes > scratch_bytes ? ring_bytes : scratch_bytes), 4);
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&rs.full[s], 1);
-      mbar_init(&rs.empty[s], kGuGroups * ncw);
+      mbar_init(&rs.empty[s], ncons_w);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&rs.red_full[s], ncons_w);
+      mbar_init(&rs.red_empty[s], 1);
     }
     rs.abort_flag = 0;
     mbar_init_fence();
   }
-  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  const int U = (int)p.ws.hdr->n_active;
+  // Zero the down kernel's per-row-tile completion counters (stream order
+  // puts this kernel's completion before the down kernel reads them).
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < (H + 31) / 32; i += blockDim.x) p.ws.rowdone[i] = 0u;
+  if (p.fused_route) {
+    // Route the batch from the router scores in scratch that aliases the
+    // (still idle) ring; CTA 0 publishes the route for the down kernel and
+    // the caller.
+    SmallPlan sp;
+    sp.ue = pl.ue;
+    sp.ub0 = pl.ub0;
+    sp.un = pl.un;
+    sp.pairs = pl.pairs;
+    route_small(p.rp, reinterpret_cast<char*>(ring_data), sp, blockIdx.x == 0);
+    pl.U = sp.U;
+    // Generic-proxy writes to the ring must be ordered before the bulk
+    // copies (async proxy) that will overwrite it.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else {
+    load_plan(p, pl);
+  }
+  __syncthreads();
+  plan_cache_ptrs(p, pl, 0);
+  __syncthreads();
   const int tiles = I / R;
-  const int n_items = U * tiles;
-  if (warp == kGuGroups * ncw) {
-    if (lane == 0) {
-      ring_produce(rs, smem, stages, stage_bytes, p.ws.hdr,
+  const int n_items = pl.U * tiles;
+
+  if (warp == ncons_w + 1) {  // producer
+    if (lane == 0)
+      ring_produce(rs, ring_data, stages, stage_bytes, p.ws.hdr,
                    [&]() {
                      const int item = (int)atomicAdd(&p.ws.hdr->queue[kQGateUp], 1u);
                      return item < n_items ? item : -1;
                    },
                    [&](int item, uint8_t* st, uint64_t* bar) {
                      const int u = item / tiles, rt = item % tiles;
-                     const moe_expert ex = p.experts[p.ws.act_e[u]];
+                     const uint8_t* const* pp = pl.ptrs + u * 4;
                      const size_t r0 = (size_t)rt * R;
-                     if (!expert_ptrs_ok(ex)) {
-                       set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+                     if (!pp[0]) {  // bad descriptor: flagged in the plan, not read
                        mbar_arrive(bar);
                        return;
                      }
                      mbar_arrive_expect_tx(bar, 2 * qbytes + 2 * sbytes);
-                     bulk_g2s(st, ex.gate.q + r0 * qrow, qbytes, bar);
-                     bulk_g2s(st + qbytes, ex.up.q + r0 * qrow, qbytes, bar);
-                     bulk_g2s(st + 2 * qbytes, ex.gate.s + r0 * nbH, sbytes, bar);
-                     bulk_g2s(st + 2 * qbytes + sbytes, ex.up.s + r0 * nbH, sbytes, bar);
+                     bulk_g2s(st, pp[0] + r0 * qrow, qbytes, bar);
+                     bulk_g2s(st + qbytes, pp[1] + r0 * qrow, qbytes, bar);
+                     bulk_g2s(st + 2 * qbytes, pp[2] + r0 * nbH, sbytes, bar);
+                     bulk_g2s(st + 2 * qbytes + sbytes, pp[3] + r0 * nbH, sbytes, bar);
                    });
+    return;
+  }
+
+  float* hout = reinterpret_cast<float*>(p.ws.h);
+  if (warp == ncons_w) {  // reducer
+    for (int pc = 0;; ++pc) {
+      const int slot = pc & 1;
+      if (!mbar_wait(&rs.red_full[slot], (pc >> 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        break;
+      }
+      const GuRedMeta m = rmeta[slot];
+      if (m.r0 < 0) break;
+      const int grp = lane / kGuTmaVals, v = lane % kGuTmaVals;
+      float sum = 0.f;
+      if (lane < kGuGroups * kGuTmaVals)
+        for (int w = 0; w < ncw; ++w) sum += red[slot][grp * ncw + w][v];
+      const float other = __shfl_down_sync(0xFFFFFFFFu, sum, RG * NT);
+      if (lane < kGuGroups * kGuTmaVals && v < RG * NT) {
+        const int r = v / NT, i = v % NT;
+        const int row = m.r0 + grp + kGuGroups * r;
+        if (m.ent[i] >= 0) {
+          const float g = sum * m.inv[i], u = other * m.inv[i];
+          hout[(size_t)m.ent[i] * I + h_swz(row)] = silu_f32(g) * u;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_empty[slot]);
     }
     return;
   }
+
+  // consumers
   const int grp = warp / ncw;
+  const int gw = warp - grp * ncw;
   const int tau = threadIdx.x - grp * ncw * 32;  // block column
   const bool col = tau < nbH;
-  const int gw = warp - grp * ncw;                // warp index inside the group
-  float* hout = reinterpret_cast<float*>(p.ws.h);
-  float xr[NT][32];
+  float xr[NT][32];       // fp32 activations (fp32 input)
+  uint32_t xh[NT][16];    // scaled f16 pairs (bf16 input)
+  float inv[NT];
   int xt[NT];
 #pragma unroll
-  for (int i = 0; i < NT; ++i) xt[i] = -2;
+  for (int i = 0; i < NT; ++i) { xt[i] = -2; inv[i] = 1.f; }
+  int pc = 0;
   for (int it = 0;; ++it) {
     const int s = it % stages, use = it / stages;
     if (!mbar_wait(&rs.full[s], use & 1)) {
@@ -455,36 +666,66 @@ __global__ void __launch_bounds__(544, 1) k_dec_gateup_tma(ExpertParams p, int s
     const int item = rs.item[s];
     if (item < 0) break;
     const int u = item / tiles, rt = item % tiles;
-    const int e = p.ws.act_e[u];
-    const int b0 = p.offsets[e], n = p.offsets[e + 1] - b0;
+    const int b0 = pl.ub0[u], n = pl.un[u];
     const int r0 = rt * R;
-    const uint8_t* st = smem + (size_t)s * stage_bytes;
+    const uint8_t* st = ring_data + (size_t)s * stage_bytes;
+    bool dead = false;
     for (int pass = 0; pass < n; pass += NT) {
       int pe[NT];
+      bool reload = false;
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        pe[i] = pass + i < n ? p.sorted[b0 + pass + i] : -1;
-        if (pe[i] >= p.T * k) {
-          set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
-          pe[i] = -1;
-        }
+        pe[i] = pass + i < n ? pl.pairs[b0 + pass + i] : -1;
         const int t = pe[i] >= 0 ? pe[i] / k : -1;
-        if (t != xt[i]) {
+        reload |= t != xt[i];
+      }
+      if (reload) {
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const int t = pe[i] >= 0 ? pe[i] / k : -1;
+          float v[32];
           if (col && t >= 0)
-            load_act_block<XBF16>(p.x, (int64_t)t * H + (int64_t)tau * 32, xr[i]);
+            load_act_block<XBF16>(p.x, (int64_t)t * H + (int64_t)tau * 32, v);
           else
 #pragma unroll
-            for (int c = 0; c < 32; ++c) xr[i][c] = 0.f;
+            for (int c = 0; c < 32; ++c) v[c] = 0.f;
           xt[i] = t;
+          if (XBF16) {
+            float m = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) m = fmaxf(m, fabsf(v[c]));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (lane == 0) gmax[grp][gw] = m;
+            named_sync(2 + grp, ncw * 32);
+            m = 0.f;
+            for (int w = 0; w < ncw; ++w) m = fmaxf(m, gmax[grp][w]);
+            named_sync(2 + grp, ncw * 32);
+            // sigma: largest magnitude scaled into [2^12, 2^13).
+            int sig = 0;
+            if (m > 0.f) sig = 12 - ((int)((__float_as_uint(m) >> 23) & 0xFF) - 127);
+            sig = sig > 100 ? 100 : (sig < -100 ? -100 : sig);
+            const float up = __int_as_float((sig + 127) << 23);
+            inv[i] = __int_as_float((127 - sig) << 23);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const __half2 h2 = __floats2half2_rn(v[2 * c] * up, v[2 * c + 1] * up);
+              xh[i][c] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) xr[i][c] = v[c];
+            inv[i] = 1.f;
+          }
         }
       }
-      float acc[kGuGroupVals];
+      float acc[kGuTmaVals];
 #pragma unroll
-      for (int v = 0; v < kGuGroupVals; ++v) acc[v] = 0.f;
+      for (int v = 0; v < kGuTmaVals; ++v) acc[v] = 0.f;
       if (col) {
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
-          const int rl = grp + kGuGroups * r;  // local row in the tile
+          const int rl = grp + kGuGroups * r;
           const uint4 gq = lds128(st + (size_t)rl * qrow + (size_t)tau * 16);
           const uint4 uq = lds128(st + qbytes + (size_t)rl * qrow + (size_t)tau * 16);
           const uint32_t gs = st[2 * qbytes + rl * nbH + tau];
@@ -492,8 +733,13 @@ __global__ void __launch_bounds__(544, 1) k_dec_gateup_tma(ExpertParams p, int s
           float ag[NT], au[NT];
 #pragma unroll
           for (int i = 0; i < NT; ++i) { ag[i] = 0.f; au[i] = 0.f; }
-          mx_block_dot<NT>(gq, gs, xr, ag);
-          mx_block_dot<NT>(uq, us, xr, au);
+          if (XBF16) {
+            mx_block_dot_f16<NT>(gq, gs, xh, ag);
+            mx_block_dot_f16<NT>(uq, us, xh, au);
+          } else {
+            mx_block_dot<NT>(gq, gs, xr, ag);
+            mx_block_dot<NT>(uq, us, xr, au);
+          }
 #pragma unroll
           for (int i = 0; i < NT; ++i) {
             acc[r * NT + i] = ag[i];
@@ -501,83 +747,195 @@ __global__ void __launch_bounds__(544, 1) k_dec_gateup_tma(ExpertParams p, int s
           }
         }
       }
-      const float tot = warp_transpose_reduce<kGuGroupVals>(acc);
-      if (lane < kGuGroupVals) red[warp][lane] = tot;
-      named_sync(1, ncons);
-      if (gw == 0) {
-        float v = 0.f;
-        if (lane < kGuGroupVals)
-          for (int w = 0; w < ncw; ++w) v += red[grp * ncw + w][lane];
-        const float uval = __shfl_down_sync(0xFFFFFFFFu, v, RG * NT);
-        if (lane < RG * NT) {
-          const int r = lane / NT, i = lane % NT;
-          const int row = r0 + grp + kGuGroups * r;
-          if (pe[i] >= 0) hout[(size_t)pe[i] * I + row] = silu_f32(v) * uval;
-        }
+      const float tot = warp_transpose_reduce<kGuTmaVals>(acc);
+      const int slot = pc & 1;
+      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        dead = true;
+        break;
       }
-      named_sync(1, ncons);
+      if (lane < kGuTmaVals) red[slot][warp][lane] = tot;
+      if (warp == 0 && lane == 0) {
+        GuRedMeta m;
+        m.r0 = r0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          m.ent[i] = i < NT ? pe[i < NT ? i : 0] : -1;
+          m.inv[i] = i < NT ? inv[i < NT ? i : 0] : 1.f;
+        }
+        rmeta[slot] = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+      ++pc;
     }
+    if (dead) break;
     __syncwarp();
     if (lane == 0) mbar_arrive(&rs.empty[s]);
   }
+  // Tell the reducer there is no more work.
+  {
+    const int slot = pc & 1;
+    if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
+    if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+  }
 }
 
-// Down.  Item = (active expert u, tile of 4G rows of Wd); thread
-// tau = g * (I/32) + b owns block column b of local rows r*G + g.
+// -------------------------------------------------------- down + combine --
+// Item = (active expert u, tile of 64 rows of Wd), one contiguous bulk copy.
+// Warp w owns block columns 4w..4w+3 of all 64 rows; lane l owns block column
+// 4w + (l & 3) of local rows r*8 + g, g = 2*(l >> 3) + ((l >> 2) & 1), so a
+// quarter-warp reads one even and one odd 704-byte row x 4 consecutive 16-byte
+// chunks: 8 distinct bank groups, no conflict.  The warp's sum over its 4
+// block columns is two xor-shuffle steps; the reducer adds the warps in
+// order.  h of the item's first NT pairs is staged by the producer.  When all
+// active experts have written a row tile, the reducer that finished last
+// combines it into out in slot order.
+constexpr int kDnG = 8;                 // row groups
+constexpr int kDnRPG = 8;               // rows per group
+constexpr int kDnRows = kDnG * kDnRPG;  // rows per item
+
+struct DnRedMeta {
+  int r0;
+  int rt;
+  int last;  // 1 on the item's last pass
+  int ent[2];
+};
+
 template <int NT>
-__global__ void __launch_bounds__(416, 1) k_dec_down_tma(ExpertParams p, int G, int stages, uint32_t stage_bytes) {
+__global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int stages, uint32_t stage_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ RingSmem rs;
-  __shared__ float part[384 * kDnRowsPerGroup * NT];
-  const int H = p.H, I = p.I;
+  __shared__ Ring rs;
+  __shared__ float red[2][12][kDnRows * NT];
+  __shared__ DnRedMeta rmeta[2];
+  const int H = p.H, I = p.I, k = p.k, T = p.T;
   const int nbI = I / 32;
-  const int nthr = G * nbI;
-  const int ncons = ((nthr + 31) / 32) * 32;
-  const int rows_per_item = G * kDnRowsPerGroup;
+  const int ncons = nbI * kDnG;                // multiple of 32 when nbI % 4 == 0
+  const int ncons_w = ncons / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t qrow = (size_t)I / 2;
-  const uint32_t qbytes = (uint32_t)(rows_per_item * qrow), sbytes = (uint32_t)(rows_per_item * nbI);
+  const uint32_t qbytes = (uint32_t)(kDnRows * qrow), sbytes = (uint32_t)(kDnRows * nbI);
+  const uint32_t hbytes = (uint32_t)(I * 4);
+  uint8_t* ring_data = smem;
+  Plan pl = plan_carve(p, smem + (size_t)stages * stage_bytes, 2);
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&rs.full[s], 1);
-      mbar_init(&rs.empty[s], ncons / 32);
+      mbar_init(&rs.empty[s], ncons_w);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&rs.red_full[s], ncons_w);
+      mbar_init(&rs.red_empty[s], 1);
     }
     rs.abort_flag = 0;
     mbar_init_fence();
   }
-  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  const int U = (int)p.ws.hdr->n_active;
-  const int tiles = H / rows_per_item;
-  const int n_items = U * tiles;
-  if (warp == ncons / 32) {
-    if (lane == 0) {
-      ring_produce(rs, smem, stages, stage_bytes, p.ws.hdr,
+  load_plan(p, pl);
+  __syncthreads();
+  plan_cache_ptrs(p, pl, 1);
+  __syncthreads();
+  const int tiles = H / kDnRows;
+  const int n_items = pl.U * tiles;
+  const float* hin = reinterpret_cast<const float*>(p.ws.h);
+
+  if (warp == ncons_w + 1) {  // producer
+    if (lane == 0)
+      ring_produce(rs, ring_data, stages, stage_bytes, p.ws.hdr,
                    [&]() {
                      const int item = (int)atomicAdd(&p.ws.hdr->queue[kQDown], 1u);
                      return item < n_items ? item : -1;
                    },
                    [&](int item, uint8_t* st, uint64_t* bar) {
                      const int u = item / tiles, rt = item % tiles;
-                     const moe_expert ex = p.experts[p.ws.act_e[u]];
-                     const size_t r0 = (size_t)rt * rows_per_item;
-                     if (!expert_ptrs_ok(ex)) {
-                       set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+                     const uint8_t* const* pp = pl.ptrs + u * 2;
+                     const size_t r0 = (size_t)rt * kDnRows;
+                     if (!pp[0]) {  // bad descriptor: flagged in the plan, not read
                        mbar_arrive(bar);
                        return;
                      }
-                     mbar_arrive_expect_tx(bar, qbytes + sbytes);
-                     bulk_g2s(st, ex.down.q + r0 * qrow, qbytes, bar);
-                     bulk_g2s(st + qbytes, ex.down.s + r0 * nbI, sbytes, bar);
+                     const int b0 = pl.ub0[u], n = pl.un[u];
+                     int nh = 0;
+                     for (int i = 0; i < NT && i < n; ++i) nh += pl.pairs[b0 + i] >= 0 ? 1 : 0;
+                     mbar_arrive_expect_tx(bar, qbytes + sbytes + nh * hbytes);
+                     bulk_g2s(st, pp[0] + r0 * qrow, qbytes, bar);
+                     bulk_g2s(st + qbytes, pp[1] + r0 * nbI, sbytes, bar);
+                     for (int i = 0; i < NT && i < n; ++i) {
+                       const int pe = pl.pairs[b0 + i];
+                       if (pe >= 0) bulk_g2s(st + qbytes + sbytes + i * hbytes, hin + (size_t)pe * I, hbytes, bar);
+                     }
                    });
+    return;
+  }
+
+  if (warp == ncons_w) {  // reducer (+ combine)
+    for (int pc = 0;; ++pc) {
+      const int slot = pc & 1;
+      if (!mbar_wait(&rs.red_full[slot], (pc >> 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        break;
+      }
+      const DnRedMeta m = rmeta[slot];
+      if (m.r0 < 0) break;
+      // lane owns output rows lane and lane + 32; NT pairs each.
+#pragma unroll
+      for (int h2 = 0; h2 < kDnRows / 32; ++h2)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const int rl = lane + 32 * h2;
+          float sum = 0.f;
+          for (int w = 0; w < ncons_w; ++w) sum += red[slot][w][rl * NT + i];
+          if (m.ent[i] >= 0) p.ws.y[(size_t)m.ent[i] * H + m.r0 + rl] = sum;
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_empty[slot]);
+      if (m.last) {
+        __threadfence();
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) prev = atomicAdd(&p.ws.rowdone[m.rt], 1u);
+        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+        if (prev == (unsigned)pl.U - 1) {
+          __threadfence();
+          // Last expert of this row tile: out[t][row] in slot order.
+          for (int h2 = 0; h2 < kDnRows / 32; ++h2)
+          for (int t = 0; t < T; ++t) {
+            const int row = m.r0 + lane + 32 * h2;
+            float yv[kMaxK], wv[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+              if (j < k) {
+                yv[j] = __ldcg(&p.ws.y[(size_t)(t * k + j) * H + row]);
+                wv[j] = __ldg(&p.w[t * k + j]);
+              }
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j)
+              if (j < k) acc = fmaf(wv[j], yv[j], acc);
+            float* o = p.out + (size_t)t * H + row;
+            if (p.accumulate) acc += *o;
+            *o = acc;
+          }
+        }
+      }
     }
     return;
   }
-  const int tau = threadIdx.x;
-  const int g = tau / nbI, b = tau % nbI;
-  const bool act = tau < nthr;
-  const float* hin = reinterpret_cast<const float*>(p.ws.h);
+
+  // consumers
+  const int b = 4 * warp + (lane & 3);
+  const int g = 2 * (lane >> 3) + ((lane >> 2) & 1);
+  float hr[NT][32];
+  int hcur[NT];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) hcur[i] = -2;
+  int pc = 0;
   for (int it = 0;; ++it) {
     const int s = it % stages, use = it / stages;
     if (!mbar_wait(&rs.full[s], use & 1)) {
@@ -588,122 +946,170 @@ __global__ void __launch_bounds__(416, 1) k_dec_down_tma(ExpertParams p, int G, 
     const int item = rs.item[s];
     if (item < 0) break;
     const int u = item / tiles, rt = item % tiles;
-    const int e = p.ws.act_e[u];
-    const int b0 = p.offsets[e], n = p.offsets[e + 1] - b0;
-    const int r0 = rt * rows_per_item;
-    const uint8_t* st = smem + (size_t)s * stage_bytes;
+    const int b0 = pl.ub0[u], n = pl.un[u];
+    const int r0 = rt * kDnRows;
+    const uint8_t* st = ring_data + (size_t)s * stage_bytes;
+    bool dead = false;
     for (int pass = 0; pass < n; pass += NT) {
       int pe[NT];
-      float hr[NT][32];
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        pe[i] = pass + i < n ? p.sorted[b0 + pass + i] : -1;
-        if (pe[i] >= p.T * p.k) {
-          set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
-          pe[i] = -1;
+        pe[i] = pass + i < n ? pl.pairs[b0 + pass + i] : -1;
+        if (pe[i] != hcur[i]) {
+          if (pe[i] < 0) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) hr[i][c] = 0.f;
+          } else {
+            // Block b of the interleaved h: chunk c at float4 (b/4)*32 + c*4 + b%4.
+            const float4* src = pass == 0 ? reinterpret_cast<const float4*>(st + qbytes + sbytes + i * hbytes)
+                                          : reinterpret_cast<const float4*>(hin + (size_t)pe[i] * I);
+            src += (b >> 2) * 32 + (b & 3);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float4 v = src[c * 4];
+              hr[i][4 * c] = v.x; hr[i][4 * c + 1] = v.y; hr[i][4 * c + 2] = v.z; hr[i][4 * c + 3] = v.w;
+            }
+          }
+          hcur[i] = pe[i];
         }
-        if (act && pe[i] >= 0)
-          load_act_block<false>(hin, (int64_t)pe[i] * I + (int64_t)b * 32, hr[i]);
-        else
-#pragma unroll
-          for (int c = 0; c < 32; ++c) hr[i][c] = 0.f;
       }
-      if (act) {
-        float acc[kDnRowsPerGroup][NT];
+      float acc[kDnRPG][NT];
 #pragma unroll
-        for (int r = 0; r < kDnRowsPerGroup; ++r)
+      for (int r = 0; r < kDnRPG; ++r)
 #pragma unroll
-          for (int i = 0; i < NT; ++i) acc[r][i] = 0.f;
+        for (int i = 0; i < NT; ++i) acc[r][i] = 0.f;
 #pragma unroll
-        for (int r = 0; r < kDnRowsPerGroup; ++r) {
-          const int rl = r * G + g;
-          const uint4 q = lds128(st + (size_t)rl * qrow + (size_t)b * 16);
-          const uint32_t sc = st[qbytes + rl * nbI + b];
-          mx_block_dot<NT>(q, sc, hr, acc[r]);
+      for (int r = 0; r < kDnRPG; ++r) {
+        const int rl = r * kDnG + g;
+        const uint4 q = lds128(st + (size_t)rl * qrow + (size_t)b * 16);
+        const uint32_t sc = st[qbytes + rl * nbI + b];
+        mx_block_dot<NT>(q, sc, hr, acc[r]);
+      }
+      // Sum the warp's 4 block columns (lanes with equal g): xor 1, xor 2.
+#pragma unroll
+      for (int r = 0; r < kDnRPG; ++r)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          float v = acc[r][i];
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+          acc[r][i] = v;
         }
-#pragma unroll
-        for (int r = 0; r < kDnRowsPerGroup; ++r)
-#pragma unroll
-          for (int i = 0; i < NT; ++i) part[(size_t)tau * (kDnRowsPerGroup * NT) + r * NT + i] = acc[r][i];
+      const int slot = pc & 1;
+      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        dead = true;
+        break;
       }
-      named_sync(1, ncons);
-      for (int o = threadIdx.x; o < rows_per_item * NT; o += ncons) {
-        const int i = o % NT, rr = o / NT;
-        const int gg = rr % G, r = rr / G;
-        float sum = 0.f;
-        for (int bb = 0; bb < nbI; ++bb) sum += part[(size_t)(gg * nbI + bb) * (kDnRowsPerGroup * NT) + r * NT + i];
-        if (pe[i] >= 0) p.ws.y[(size_t)pe[i] * H + r0 + r * G + gg] = sum;
+      if ((lane & 3) == 0) {
+#pragma unroll
+        for (int r = 0; r < kDnRPG; ++r)
+#pragma unroll
+          for (int i = 0; i < NT; ++i) red[slot][warp][(r * kDnG + g) * NT + i] = acc[r][i];
       }
-      named_sync(1, ncons);
+      if (warp == 0 && lane == 0) {
+        DnRedMeta m;
+        m.r0 = r0;
+        m.rt = rt;
+        m.last = pass + NT >= n ? 1 : 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) m.ent[i] = i < NT ? pe[i < NT ? i : 0] : -1;
+        rmeta[slot] = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+      ++pc;
     }
+    if (dead) break;
     __syncwarp();
     if (lane == 0) mbar_arrive(&rs.empty[s]);
   }
-}
-
-// Stages that fit the dynamic shared memory budget (>= 2).
-static int ring_stages(uint32_t stage_bytes, size_t budget) {
-  int n = (int)(budget / stage_bytes);
-  return n > kMaxStages ? kMaxStages : n;
+  {
+    const int slot = pc & 1;
+    if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
+    if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+  }
 }
 
 template <int NT>
-static bool tma_path_ok(const ExpertParams& p, int G) {
-  const int R = 8 / NT;
+static bool tma_path_ok(const ExpertParams& p) {
+  const int R = kGuRowsNT / NT;
   const int nbH = p.H / 32, nbI = p.I / 32;
-  const int rd = G * kDnRowsPerGroup;
-  return (R * nbH) % 16 == 0 && (rd * nbI) % 16 == 0 && p.H % rd == 0 && (G & (G - 1)) == 0 &&
-         G * nbI <= 384 && nbH <= 256;
+  return p.T * p.k <= kMaxPairs && plan_smem_bytes(p.E, p.T * p.k, 4) <= 48 * 1024 && (R * nbH) % 16 == 0 &&
+         nbI % 4 == 0 && nbI <= 48 && nbH <= 256 && p.H % kDnRows == 0 && (kDnRows * nbI) % 16 == 0 &&
+         p.k <= kMaxK && p.E <= 4096;
 }
 
 template <int NT>
 static cudaError_t launch_decode_tma(const ExpertParams& p, cudaStream_t s) {
-  constexpr int R = 8 / NT;
+  constexpr int R = kGuRowsNT / NT;
   const int nsm = device_sm_count();
-  const size_t budget = 200 * 1024;
   cudaError_t err;
-  // gate/up
+  const size_t smem_max = 200 * 1024;
+  // gate/up (+ routing prologue)
   const int nbH = p.H / 32;
   const int ncw = (nbH + 31) / 32;
+  const int gu_threads = kGuGroups * ncw * 32 + 64;
+  const size_t gu_plan = plan_smem_bytes(p.E, p.T * p.k, 4);
   const uint32_t gu_stage = (uint32_t)(2 * R * (p.H / 2) + 2 * R * nbH);
-  const int gu_stages = ring_stages(gu_stage, budget);
+  int gu_stages = (int)((smem_max - gu_plan) / gu_stage);
+  gu_stages = gu_stages > kMaxStages ? kMaxStages : gu_stages;
+  if (gu_stages < 2) return cudaErrorNotSupported;
+  size_t gu_front = (size_t)gu_stages * gu_stage;
+  if (p.fused_route) {
+    const size_t scratch = route_small_scratch_bytes(p.E, gu_threads / 32, p.T);
+    if (scratch > gu_front) gu_front = scratch;
+  }
+  const size_t gu_smem = gu_front + gu_plan;
+  if (gu_smem > smem_max) return cudaErrorNotSupported;
   auto gu = p.x_bf16 ? k_dec_gateup_tma<NT, true> : k_dec_gateup_tma<NT, false>;
-  const size_t gu_smem = (size_t)gu_stages * gu_stage;
   if ((err = ensure_smem_attr((const void*)gu, gu_smem)) != cudaSuccess) return err;
   prof_before(MOE_STAGE_GATEUP, s);
-  err = launch_pdl(gu, dim3(nsm), dim3(kGuGroups * ncw * 32 + 32), gu_smem, s, p, gu_stages, gu_stage);
+  err = launch_pdl(gu, dim3(nsm), dim3(gu_threads), gu_smem, s, p, gu_stages, gu_stage);
   prof_after(MOE_STAGE_GATEUP, s);
   if (err != cudaSuccess) return err;
-  // down
-  int G = down_groups(p.I);
-  while (G & (G - 1)) --G;
+  // down (+ combine)
   const int nbI = p.I / 32;
-  const int rd = G * kDnRowsPerGroup;
-  const uint32_t dn_stage = (uint32_t)(rd * (p.I / 2) + rd * nbI);
-  const int dn_stages = ring_stages(dn_stage, budget);
-  const size_t dn_smem = (size_t)dn_stages * dn_stage;
+  const size_t dn_plan = plan_smem_bytes(p.E, p.T * p.k, 2);
+  const uint32_t dn_stage = (uint32_t)(kDnRows * (p.I / 2) + kDnRows * nbI + NT * p.I * 4);
+  int dn_stages = (int)((smem_max - dn_plan) / dn_stage);
+  dn_stages = dn_stages > kMaxStages ? kMaxStages : dn_stages;
+  if (dn_stages < 2) return cudaErrorNotSupported;
+  const size_t dn_smem = (size_t)dn_stages * dn_stage + dn_plan;
   auto dn = k_dec_down_tma<NT>;
   if ((err = ensure_smem_attr((const void*)dn, dn_smem)) != cudaSuccess) return err;
-  const int ncons = ((G * nbI + 31) / 32) * 32;
   prof_before(MOE_STAGE_DOWN, s);
-  err = launch_pdl(dn, dim3(nsm), dim3(ncons + 32), dn_smem, s, p, G, dn_stages, dn_stage);
+  err = launch_pdl(dn, dim3(nsm), dim3(nbI * kDnG + 64), dn_smem, s, p, dn_stages, dn_stage);
   prof_after(MOE_STAGE_DOWN, s);
-  if (err != cudaSuccess) return err;
-  const int64_t n4 = (int64_t)p.T * (p.H / 4);
-  int cgrid = (int)((n4 + 255) / 256);
-  if (cgrid > nsm * 8) cgrid = nsm * 8;
-  prof_before(MOE_STAGE_COMBINE, s);
-  err = launch_pdl(k_dec_combine, dim3(cgrid), dim3(256), 0, s, p);
-  prof_after(MOE_STAGE_COMBINE, s);
   return err;
 }
 
 template <int NT>
 static cudaError_t launch_decode_nt(const ExpertParams& p, cudaStream_t s) {
-  int G = down_groups(p.I);
-  while (G & (G - 1)) --G;
-  if (tma_path_ok<NT>(p, G)) return launch_decode_tma<NT>(p, s);
+  if (tma_path_ok<NT>(p)) return launch_decode_tma<NT>(p, s);
   return launch_decode_ldg<NT>(p, s);
+}
+
+// The whole decode layer: router scores, then (when the staged kernels apply)
+// gate/up with the routing fused into its prologue and down + combine;
+// otherwise the standalone routing kernels and the register-streaming path.
+cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s) {
+  const bool small_route = route_decode_supported(rp.T, rp.H, rp.E, rp.k);
+  const bool staged = p.T == 1 ? tma_path_ok<1>(p) : tma_path_ok<2>(p);
+  if (small_route && staged) {
+    cudaError_t err = launch_router_gemv(rp, s);
+    if (err != cudaSuccess) return err;
+    p.fused_route = 1;
+    p.rp = rp;
+    return p.T == 1 ? launch_decode_tma<1>(p, s) : launch_decode_tma<2>(p, s);
+  }
+  cudaError_t err = small_route ? launch_route_decode(rp, s) : launch_route_prefill(rp, bp, s);
+  if (err != cudaSuccess) return err;
+  p.fused_route = 0;
+  return launch_decode_experts(p, s);
 }
 
 // NT = routed pairs of one expert processed per weight pass.  The choice

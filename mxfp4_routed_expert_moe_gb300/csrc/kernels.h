@@ -48,6 +48,8 @@ inline void prof_after(int stage, cudaStream_t s) {
 
 // route.cu
 bool route_decode_supported(int T, int H, int E, int k);
+size_t small_plan_bytes(int E, int npairs);
+cudaError_t launch_router_gemv(const RouteParams& p, cudaStream_t s);
 cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s);
 cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s);
 cudaError_t launch_bucket_from_ids(const BucketParams& b, cudaStream_t s);
@@ -55,6 +57,7 @@ cudaError_t launch_plan_from_offsets(const BucketParams& b, const int32_t* offse
 
 // decode.cu
 cudaError_t launch_decode_experts(const ExpertParams& p, cudaStream_t s);
+cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s);
 
 // prefill.cu
 constexpr int kPfNTile = 128;   // tokens per MMA tile (N)

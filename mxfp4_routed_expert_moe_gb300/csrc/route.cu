@@ -10,68 +10,11 @@
 // next-layer expert prefetch"].
 #include <utility>
 
+#include "async.cuh"
 #include "kernels.h"
+#include "route_small.cuh"
 
 namespace moe {
-
-constexpr uint32_t kTaken = 0xFFFFFFFFu;  // hi bits of an already selected expert
-
-__device__ __forceinline__ uint32_t ord32(float f) {
-  const uint32_t b = __float_as_uint(f + 0.0f);  // -0 -> +0
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);  // monotone in f
-}
-
-// Orderable key of a double-float score (hi, lo): value order, with a taken
-// entry (hi bits kTaken) below every real score.
-__device__ __forceinline__ unsigned long long score_key(float2 v) {
-  if (__float_as_uint(v.x) == kTaken) return 0ull;
-  return ((unsigned long long)ord32(v.x) << 32) | ord32(v.y);
-}
-
-// Top-k of one token by one warp over its double-float scores in shared
-// memory `row` (destroyed): larger score first, lower expert index on equal
-// scores.  Lane j < k returns slot j's expert and score.
-__device__ __forceinline__ void warp_topk(float2* row, int E, int k, int& my_e, float2& my_s) {
-  const int lane = threadIdx.x & 31;
-  my_e = -1;
-  my_s = make_float2(0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
-    int best_e = 0x7FFFFFFF;
-    for (int e = lane; e < E; e += 32) {
-      const unsigned long long kk = score_key(row[e]);
-      if (kk > best) { best = kk; best_e = e; }
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-      const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, m);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, best_e, m);
-      if (ok > best || (ok == best && oe < best_e)) { best = ok; best_e = oe; }
-    }
-    if (lane == j) {
-      my_e = best_e;
-      my_s = row[best_e];
-    }
-    __syncwarp();
-    if (lane == 0) row[best_e].x = __uint_as_float(kTaken);
-    __syncwarp();
-  }
-}
-
-// Softmax of the selected scores held by lanes 0..k-1 (slot order): lane j
-// gets exp(s_j - s_0) / sum_i exp(s_i - s_0), the differences taken from the
-// double-float scores.
-__device__ __forceinline__ float warp_route_weight(float2 my_s, int k) {
-  const int lane = threadIdx.x & 31;
-  const float h0 = __shfl_sync(0xFFFFFFFFu, my_s.x, 0);
-  const float l0 = __shfl_sync(0xFFFFFFFFu, my_s.y, 0);
-  const float d = (my_s.x - h0) + (my_s.y - l0);
-  const float ex = lane < k ? expf(d) : 0.0f;
-  float z = ex;
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, m);
-  return ex / z;
-}
 
 // Exclusive scan of per-expert counts (held in ws.offsets[0..E) on entry) into
 // ws.offsets (and the caller's copy), plus the active-expert list and the
@@ -134,11 +77,12 @@ __device__ void plan_scan(const BucketParams& p) {
 
 // ------------------------------------------------------ decode router GEMV --
 // s[t][e] = sum_h x[t][h] * Wr[e][h] (+ b[e]) for T <= 64, H <= 8192.  Each CTA
-// owns 4 rows of Wr and walks the tokens in pairs; thread tau holds the
-// activations of columns 4*tau + 1024*i in registers.  Eight values (4 rows x
-// 2 tokens) are reduced per warp, so every score is summed by the same tree
-// whatever T is: a token's route does not depend on the rest of the batch.
-constexpr int kRgRows = 4;
+// bulk-copies 2 contiguous rows of Wr (57 KB at H = 7168) into shared memory
+// while its threads load the activations, then walks the tokens in pairs;
+// thread tau handles columns 4*tau + 1024*i.  Four values (2 rows x 2 tokens)
+// are reduced per warp in double-float, so every score is summed by the same
+// tree whatever T is: a token's route does not depend on the rest of the batch.
+constexpr int kRgRows = 2;
 constexpr int kRgThreads = 256;
 constexpr int kRgChunks = 8;  // float4 chunks per thread per row: H <= 8192
 
@@ -153,95 +97,26 @@ __device__ __forceinline__ float4 load_x4(const void* x, int64_t idx) {
   }
 }
 
-// Single-CTA tail: top-k and bucketing of T <= 64 tokens (E <= 4096) from the
-// scores in ws.logits.  Writes ids, w, offsets, sorted (workspace and caller
-// copies) and the active-expert list.
-__device__ void route_tail_small(const RouteParams& p, char* smem) {
-  const int T = p.T, E = p.E, k = p.k;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  unsigned long long* tmask = reinterpret_cast<unsigned long long*>(smem);  // [E] token bits
-  int* cnt = reinterpret_cast<int*>(tmask + E);                             // [E]
-  int* off = cnt + E;                                                        // [E+1]
-  int* s_ids = off + E + 1;                                                  // [T*k]
-  s_ids = reinterpret_cast<int*>((reinterpret_cast<uintptr_t>(s_ids) + 15) & ~(uintptr_t)15);
-  float2* rows = reinterpret_cast<float2*>(s_ids + kDecodeMaxT * kMaxK);     // [nwarps][E]
-  for (int e = threadIdx.x; e < E; e += blockDim.x) tmask[e] = 0ull;
-  __syncthreads();
-  for (int t = warp; t < T; t += nwarps) {
-    float2* row = rows + (size_t)warp * E;
-    for (int e = lane; e < E; e += 32) row[e] = __ldcg(&p.ws.logits[(size_t)t * E + e]);
-    __syncwarp();
-    int my_e;
-    float2 my_s;
-    warp_topk(row, E, k, my_e, my_s);
-    const float wt = warp_route_weight(my_s, k);
-    if (lane < k) {
-      p.ids[t * k + lane] = my_e;
-      p.w[t * k + lane] = wt;
-      s_ids[t * k + lane] = my_e;
-      atomicOr(&tmask[my_e], 1ull << t);
-    }
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = __popcll(tmask[e]);
-  __syncthreads();
-  if (warp == 0) {
-    int run = 0, nact = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int c = e < E ? cnt[e] : 0;
-      int incl = c;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, m);
-        if (lane >= m) incl += o;
-      }
-      const unsigned act = __ballot_sync(0xFFFFFFFFu, c > 0);
-      if (e < E) {
-        off[e] = run + incl - c;
-        if (c > 0) p.ws.act_e[nact + __popc(act & ((1u << lane) - 1u))] = e;
-      }
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
-      nact += __popc(act);
-    }
-    if (lane == 0) {
-      off[E] = run;
-      p.ws.hdr->n_active = (uint32_t)nact;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    p.ws.offsets[e] = off[e];
-    if (p.offsets) p.offsets[e] = off[e];
-  }
-  // Stable scatter: the rank of token t in expert e's bucket is the number of
-  // tokens below t routed to e (a token selects an expert at most once).
-  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
-    const int t = i / k;
-    const int e = s_ids[i];
-    const unsigned long long below = t == 0 ? 0ull : (tmask[e] & ((1ull << t) - 1ull));
-    const int pos = off[e] + __popcll(below);
-    p.ws.sorted[pos] = i;
-    if (p.sorted) p.sorted[pos] = i;
-  }
-}
-
-size_t route_tail_smem_bytes(int E) {
-  return (size_t)E * 8 + (size_t)E * 4 + (size_t)(E + 1) * 4 + (size_t)kDecodeMaxT * kMaxK * 4 + 16 +
-         (size_t)(kRgThreads / 32) * E * 8 + 64;
-}
-
 template <bool XBF16>
 __global__ void __launch_bounds__(kRgThreads) k_router_gemv(RouteParams p) {
-  extern __shared__ float4 dyn_smem4[];
-  __shared__ float2 red[kRgThreads / 32][8];
-  __shared__ int is_last;
+  extern __shared__ __align__(128) uint8_t rsm[];  // [kRgRows][H] fp32
+  __shared__ uint64_t bar;
+  __shared__ float2 red[kRgThreads / 32][kRgRows * 2];
   const int H = p.H, E = p.E, T = p.T;
   const int ncols4 = H / 4;
   const int e0 = blockIdx.x * kRgRows;
+  const int nrows = E - e0 < kRgRows ? E - e0 : kRgRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* wrs = reinterpret_cast<const float*>(rsm);
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(&bar, (uint32_t)(nrows * H * 4));
+    bulk_g2s(rsm, p.wr + (size_t)e0 * H, (uint32_t)(nrows * H * 4), &bar);
+  }
   pdl_trigger();
+  __syncthreads();
+  bool rows_ready = false;
   for (int tp = 0; tp < T; tp += 2) {
     float4 xr[2][kRgChunks];
 #pragma unroll
@@ -254,66 +129,84 @@ __global__ void __launch_bounds__(kRgThreads) k_router_gemv(RouteParams p) {
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+    if (!rows_ready) {
+      if (!mbar_wait(&bar, 0)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        mbar_wait(&bar, 0);  // bounded drain of the copy in flight
+        return;
+      }
+      rows_ready = true;
+    }
     // Each float4 chunk (4 products) is summed in fp32, then added into a
     // double-float accumulator; the reductions below stay double-float.
-    float ah[8], al[8];
+    float ah[4], al[4];
 #pragma unroll
-    for (int v = 0; v < 8; ++v) { ah[v] = 0.f; al[v] = 0.f; }
+    for (int v = 0; v < 4; ++v) { ah[v] = 0.f; al[v] = 0.f; }
 #pragma unroll
     for (int i = 0; i < kRgChunks; ++i) {
       const int c4 = threadIdx.x + i * kRgThreads;
       if (c4 < ncols4) {
-        float4 wv[kRgRows];
 #pragma unroll
         for (int r = 0; r < kRgRows; ++r) {
-          const int e = e0 + r < E ? e0 + r : E - 1;
-          wv[r] = __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)e * H) + c4);
-        }
-#pragma unroll
-        for (int r = 0; r < kRgRows; ++r)
+          const float4 wv = reinterpret_cast<const float4*>(wrs + (size_t)(r < nrows ? r : 0) * H)[c4];
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            float a = wv[r].x * xr[q][i].x;
-            a = fmaf(wv[r].y, xr[q][i].y, a);
-            a = fmaf(wv[r].z, xr[q][i].z, a);
-            a = fmaf(wv[r].w, xr[q][i].w, a);
+            float a = wv.x * xr[q][i].x;
+            a = fmaf(wv.y, xr[q][i].y, a);
+            a = fmaf(wv.z, xr[q][i].z, a);
+            a = fmaf(wv.w, xr[q][i].w, a);
             df_add_f(ah[r * 2 + q], al[r * 2 + q], a);
           }
+        }
       }
     }
     float th, tl;
-    warp_transpose_reduce_df<8>(ah, al, th, tl);
-    if (lane < 8) red[warp][lane] = make_float2(th, tl);
+    warp_transpose_reduce_df<4>(ah, al, th, tl);
+    if (lane < 4) red[warp][lane] = make_float2(th, tl);
     __syncthreads();
-    if (threadIdx.x < 8) {
+    if (threadIdx.x < 4) {
       float sh = 0.f, sl = 0.f;
       for (int w = 0; w < kRgThreads / 32; ++w) df_add(sh, sl, red[w][threadIdx.x].x, red[w][threadIdx.x].y, sh, sl);
       const int r = threadIdx.x >> 1, q = threadIdx.x & 1;
       const int e = e0 + r, t = tp + q;
-      if (e < E && t < T) {
+      if (r < nrows && t < T) {
         if (p.br) df_add(sh, sl, p.br[e], 0.f, sh, sl);
         p.ws.logits[(size_t)t * E + e] = make_float2(sh, sl);
       }
     }
     __syncthreads();
   }
-  // The last CTA to finish routes and buckets all tokens.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(&p.ws.hdr->route_ticket, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  route_tail_small(p, reinterpret_cast<char*>(dyn_smem4));
-  if (threadIdx.x == 0) p.ws.hdr->route_ticket = 0u;
+  if (!rows_ready) mbar_wait(&bar, 0);  // T == 0 cannot happen; keep the copy drained
+}
+
+// Standalone small-batch routing (moe_route): top-k, weights and buckets of
+// T <= 64 tokens from the scores, by one CTA.
+__global__ void __launch_bounds__(256) k_route_small(RouteParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  pdl_wait();
+  const int npairs = p.T * p.k;
+  const int umax = p.E < npairs ? p.E : npairs;
+  SmallPlan plan;
+  plan.ue = reinterpret_cast<int*>(dsm);
+  plan.ub0 = plan.ue + umax;
+  plan.un = plan.ub0 + umax;
+  plan.pairs = plan.un + umax;
+  char* scratch = reinterpret_cast<char*>(
+      (reinterpret_cast<uintptr_t>(plan.pairs + npairs) + 15) & ~(uintptr_t)15);
+  route_small(p, scratch, plan, true);
+}
+
+size_t small_plan_bytes(int E, int npairs) {
+  const int umax = E < npairs ? E : npairs;
+  return (size_t)(3 * umax + npairs) * 4;
 }
 
 bool route_decode_supported(int T, int H, int E, int k) {
   return T <= kDecodeMaxT && H <= kRgChunks * 4 * kRgThreads && E <= 4096 && k <= kMaxK;
 }
 
-cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
-  const size_t smem = route_tail_smem_bytes(p.E);
+cudaError_t launch_router_gemv(const RouteParams& p, cudaStream_t s) {
+  const size_t smem = (size_t)kRgRows * p.H * 4;
   const dim3 grid((p.E + kRgRows - 1) / kRgRows);
   auto kern = p.x_bf16 ? k_router_gemv<true> : k_router_gemv<false>;
   cudaError_t err = ensure_smem_attr((const void*)kern, smem);
@@ -322,6 +215,14 @@ cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
   kern<<<grid, kRgThreads, smem, s>>>(p);
   prof_after(MOE_STAGE_ROUTE, s);
   return cudaGetLastError();
+}
+
+cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
+  cudaError_t err = launch_router_gemv(p, s);
+  if (err != cudaSuccess) return err;
+  const size_t smem = small_plan_bytes(p.E, p.T * p.k) + 16 + route_small_scratch_bytes(p.E, 8, p.T);
+  if ((err = ensure_smem_attr((const void*)k_route_small, smem)) != cudaSuccess) return err;
+  return launch_pdl(k_route_small, dim3(1), dim3(256), smem, s, p);
 }
 
 // ------------------------------------------------------- prefill router GEMM --
@@ -413,7 +314,15 @@ __global__ void __launch_bounds__(256) k_topk(RouteParams p) {
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
   float2* row = rows + (size_t)warp * E;
-  for (int e = lane; e < E; e += 32) row[e] = p.ws.logits[(size_t)t * E + e];
+  for (int e0 = lane; e0 < E; e0 += 256) {
+    float2 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (e0 + 32 * q < E) v[q] = p.ws.logits[(size_t)t * E + e0 + 32 * q];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (e0 + 32 * q < E) row[e0 + 32 * q] = v[q];
+  }
   __syncwarp();
   int my_e;
   float2 my_s;
