@@ -45,7 +45,7 @@ int resolve_path(const moe_shape* s, int x_dtype, int path, int* out) {
   if (path == MOE_PATH_DECODE) {
     if (!decode_experts_supported(s)) return MOE_ERR_UNSUPPORTED;
   } else if (path == MOE_PATH_PREFILL) {
-    if (x_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
+    if (x_dtype != MOE_DT_BF16 || !prefill_supported(s->H, s->I)) return MOE_ERR_UNSUPPORTED;
   } else {
     return MOE_ERR_INVALID_ARG;
   }

@@ -44,7 +44,9 @@ struct Ws {
   int32_t* act_pref_dn; // [E+1]   prefix of prefill down tiles per active expert
   uint16_t* xh;         // [T][H]  fp16 activations (prefill)
   float* xscale;        // [T]     2^-sigma_t of the fp16 activations
-  void* h;              // [T*k][I] fp32 (decode) or fp16 (prefill)
+  void* h;              // [T*k][I] fp32 (decode) or [T*k + T][I] fp16 (prefill; rows
+                        // T*k.. hold the shared expert's h)
+  int32_t* shsig;       // [2I + H] row shifts of the bf16 shared expert (gate, up, down)
   float* y;             // [T*k][H] fp32 (decode, T <= 64)
   uint32_t* rowdone;    // [ceil(H/32)] per-row-tile completion counters
   size_t total;
@@ -78,8 +80,9 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.xscale = (float*)take(T * 4);
   const size_t Td = T < (size_t)kDecodeMaxT ? T : (size_t)kDecodeMaxT;
   // h: fp32 for the decode path (Td*k rows), fp16 for the prefill path (T*k rows).
-  const size_t h_dec = Td * k * I * 4, h_pf = T * k * I * 2;
+  const size_t h_dec = Td * k * I * 4, h_pf = (T * k + T) * I * 2;
   ws.h = (void*)take(h_dec > h_pf ? h_dec : h_pf);
+  ws.shsig = (int32_t*)take((2 * I + H) * 4);
   ws.y = (float*)take(Td * k * H * 4);
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
   ws.total = off;

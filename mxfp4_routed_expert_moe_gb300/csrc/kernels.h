@@ -62,6 +62,9 @@ cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp,
 // prefill.cu
 constexpr int kPfNTile = 128;   // tokens per MMA tile (N)
 constexpr int kPfMTile = 128;   // weight rows per MMA tile (M)
+// The prefill path needs H % 128 == 0 and I % 128 == 0 (64-element contraction
+// slices; 4-byte scale rows) and bf16 activations.
+bool prefill_supported(int H, int I);
 cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s);
 
 }  // namespace moe
