@@ -167,10 +167,11 @@ class Layer:
 
     def launches_per_step(self) -> int:
         # decode: router(+top-k tail), gate/up, down(+combine)
-        # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, gate/up, down (+ shared)
+        # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
+        # shifts), gate/up, down
         if self.decode_path:
             return 3  # router (+ fused top-k/bucketing), gate/up, down (+ fused combine)
-        return 7 + (2 if self.shared is not None else 0)
+        return 7 + (1 if self.shared is not None else 0)
 
     def dominant_stage(self):
         return self.moe.STAGE_GATEUP if self.decode_path else self.moe.STAGE_PF_GATEUP
@@ -190,6 +191,13 @@ class Layer:
         wl = self.wl
         xb = wl.T * wl.H * (4 if wl.x_dtype == "f32" else 2)
         return n_active * 2 * (wl.I * wl.H // 2 + wl.I * wl.H // 32) + xb + wl.T * wl.k * wl.I * 4
+
+    def flops_gateup(self) -> int:
+        """Algorithmic FLOPs of the prefill gate/up GEMM launch: routed pairs
+        (and the shared expert) x 2 matrices x H x I multiply-adds."""
+        wl = self.wl
+        rows = wl.T * wl.k + (wl.T if self.shared is not None else 0)
+        return 2 * rows * 2 * wl.H * wl.I
 
     def flops_step(self) -> int:
         return self.wl.T * self.wl.flops_per_token
@@ -505,7 +513,14 @@ def main():
                 "traffic": traffic, "kernel": "k_dec_gateup (MXFP4 gate/up GEMV + SwiGLU)",
                 "bytes_per_launch": gu_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
     else:
-        roof = None
+        fl = layer.flops_gateup()
+        achieved = fl / (st_ms / 1000.0) / 1e12
+        traffic, sha = traffic_from_profiles("pf_gateup", wl.name)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
+                "traffic": traffic, "kernel": "k_pf_gemm<gate/up> (tcgen05 kind::f16 grouped GEMM + SwiGLU)",
+                "flops_per_launch": fl, "launch_ms": st_ms,
+                "hbm_frac_of_step": layer.algorithmic_bytes_step(n_active) / (ms / 1000.0) / 1e9 / hbm,
+                "peak_source": f"{peak_src} (bf16_tflops, burst; f16 operands run at the bf16 rate)"}
     step_bytes = layer.algorithmic_bytes_step(n_active)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

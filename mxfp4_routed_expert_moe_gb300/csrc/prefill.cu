@@ -40,9 +40,25 @@ constexpr int kPfLdWarps = 4;            // warps 8-11: token rows (cp.async)
 constexpr int kPfEpWarps = 4;            // warps 12-15: epilogue (warp % 4 = TMEM lane quarter)
 constexpr int kPfMmaWarp = kPfDqWarps + kPfLdWarps + kPfEpWarps;  // warp 16: TMEM owner, MMA issuer
 constexpr int kPfThreads = (kPfMmaWarp + 1) * 32;
-constexpr int kPfBDepth = 3;             // cp.async groups in flight per loader thread
+constexpr int kPfBDepth = 4;             // cp.async groups in flight per loader thread
 constexpr int kPfMaxStages = 8;
+// Rings (per kernel): f16 weight tiles from the dequant warps (A), f16 token
+// rows from the loader warps (B), raw MXFP4 bytes of the dequant threads.
+constexpr int kPfAStagesGateUp = 2, kPfBStagesGateUp = 5;
+constexpr int kPfAStagesDown = 3, kPfBStagesDown = 6;
+constexpr int kPfL2Window = 256;         // bytes of each weight row prefetched into L2 at a time
 constexpr uint32_t kPfTmemCols = 512;    // 2 accumulator buffers x (gate 128 + up 128) columns
+constexpr int kPfSigRing = 4;            // items whose row shifts are published ahead
+// Raw MXFP4 ring of the dequant threads: per slice and thread 16 bytes of
+// codes and the 4-byte scale word per matrix, cp.async'd this many slices
+// ahead (about 48 KB in flight per SM for either kernel).
+constexpr int kPfRawGateUp = 6;
+constexpr int kPfRawDown = 12;
+template <int NA>
+struct PfRaw {
+  static constexpr int kQ = NA * kPfDqWarps * 32 * 16;   // codes
+  static constexpr int kStage = kQ + NA * kPfDqWarps * 32 * 4;  // + scale words
+};
 static_assert(kPfEpWarps == 4 && (kPfDqWarps + kPfLdWarps) % 4 == 0, "epilogue warps must cover lane quarters 0-3");
 
 // ------------------------------------------------------------ pre-passes --
@@ -232,22 +248,30 @@ __device__ __forceinline__ void dq_bf16_block(uint8_t* tile, uint32_t r, uint32_
 
 // -------------------------------------------------------- CTA control --
 struct PfShared {
-  uint64_t full[kPfMaxStages];   // stage filled: 8 dequant + 4 loader warp arrivals
-  uint64_t empty[kPfMaxStages];  // stage consumed: tcgen05.commit
+  uint64_t a_full[kPfMaxStages];   // weight tile stage filled: 8 dequant warps
+  uint64_t a_empty[kPfMaxStages];  // ... consumed: tcgen05.commit
+  uint64_t b_full[kPfMaxStages];   // token tile stage filled: 4 loader warps
+  uint64_t b_empty[kPfMaxStages];  // ... consumed: tcgen05.commit
   uint64_t accf[2];              // accumulator buffer ready: tcgen05.commit
   uint64_t acce[2];              // accumulator buffer drained: 4 epilogue warps
+  uint64_t sig_full[kPfSigRing];  // row shifts of an item published: 4 epilogue warps
+  uint64_t sig_empty[kPfSigRing]; // ... and read: 8 dequant + 4 epilogue warps
   uint32_t tmem_base;
   int abort_flag;
+  int sig[kPfSigRing][2][kPfMTile];       // row shifts (gate/down, up) of upcoming items
   float col_scale[kPfEpWarps][kPfNTile];  // per epilogue warp: token shift (gate/up) or route weight (down)
   int col_tok[kPfEpWarps][kPfNTile];      // per epilogue warp: token of each column (down)
 };
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted.  The
+// waiting thread sleeps in try_wait (at most kPfSleepNs per call) instead of
+// spinning: each SM sub-partition hosts waiting warps of several roles.
+constexpr uint32_t kPfSleepNs = 20000;
 __device__ __forceinline__ bool pf_wait(PfShared& sh, uint64_t* bar, uint32_t parity, WsHeader* hdr) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kPfSleepNs)) return true;
     if (*(volatile int*)&sh.abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       set_status(hdr, MOE_ERR_TIMEOUT);
@@ -260,9 +284,11 @@ __device__ __forceinline__ bool pf_wait(PfShared& sh, uint64_t* bar, uint32_t pa
 // Shared pipeline state of the four roles of one CTA.
 struct PfCtx {
   PfShared* sh;
-  uint8_t* smem;     // stage ring, 1024-byte aligned
-  int stages;
-  int stage_bytes;
+  uint8_t* smem_a;   // weight tile ring (NA tiles per stage), 1024-byte aligned
+  uint8_t* smem_b;   // token tile ring, 1024-byte aligned
+  uint8_t* raw;      // raw MXFP4 ring of the dequant threads
+  int a_stages, b_stages;
+  int a_bytes;       // bytes of one weight tile stage
   int n_items;       // routed + shared items
   int n_routed;
   int U;
@@ -277,136 +303,192 @@ __device__ __forceinline__ bool pf_warp_wait(const PfCtx& c, uint64_t* bar, uint
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// Claim stage of global slice gs for writing (wait until its previous use was
-// consumed by the tensor core).
-__device__ __forceinline__ bool pf_claim(const PfCtx& c, int gs) {
-  const int st = gs % c.stages, use = gs / c.stages;
+// Claim the ring stage of global slice gs for writing (wait until its
+// previous use was consumed by the tensor core).
+__device__ __forceinline__ bool pf_claim(const PfCtx& c, uint64_t* empty, int nstages, int gs) {
+  const int st = gs % nstages, use = gs / nstages;
   if (use == 0) return true;
-  return pf_warp_wait(c, &c.sh->empty[st], (use - 1) & 1);
+  return pf_warp_wait(c, &empty[st], (use - 1) & 1);
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Prefetch cursor of a dequant thread: walks the CTA's items slice by slice
+// ahead of the consumer and issues one cp.async group per slice into the raw
+// ring (an empty group for slices of the shared expert or past the end, so
+// group counts stay aligned with slices).  It also keeps the rows streaming
+// from DRAM in long runs: each weight row is prefetched into L2 in
+// kPfL2Window-byte windows eight slices ahead of the cursor, and the first
+// 512 bytes of the next item's rows near the end of the current item (the
+// per-slice copies alone read 32 bytes per row, which DRAM serves poorly).
+template <int NA>
+struct PfCursor {
+  int item, s;
+  bool mx;                 // this slice's item is a routed MXFP4 item with a valid row
+  const uint8_t* row[NA];  // codes of the row
+  const uint8_t* sw[NA];   // scale row (one 4-byte word covers two slices)
+};
+
+// Codes of weight row m0 + r of matrix a of `item`; null unless it is a
+// routed item with a valid row.
+__device__ __forceinline__ const uint8_t* item_row_codes(const ExpertParams& p, const PfCtx& c, bool gateup, int item,
+                                                         uint32_t r, int a, const uint8_t** scales) {
+  if (item >= c.n_items) return nullptr;
+  const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
+  if (it.shared) return nullptr;
+  const moe_expert ex = p.experts[it.e];
+  const int row = it.m0 + (int)r;
+  if (row >= c.M || !expert_ptrs_ok(ex)) return nullptr;
+  const moe_mx_mat m = a == 0 ? (gateup ? ex.gate : ex.down) : ex.up;
+  if (scales) *scales = m.s + (size_t)row * (c.K / 32);
+  return m.q + (size_t)row * (c.K / 2);
+}
+
+// The matrix whose L2 prefetches this thread issues (-1: none).
+template <int NA>
+__device__ __forceinline__ int prefetch_matrix(int half) {
+  return NA == 2 ? half : (half == 0 ? 0 : -1);
 }
 
 template <int NA>
-struct MxBuf {
-  uint4 q[NA];
-  uint32_t s[NA];
-};
-
-template <int NA>
-__device__ __forceinline__ void mx_load(MxBuf<NA>& b, const uint8_t* const (&qp)[NA], const uint8_t* const (&sp)[NA],
-                                        int s) {
+__device__ __forceinline__ void cursor_enter(PfCursor<NA>& cur, const ExpertParams& p, const PfCtx& c, bool gateup,
+                                             uint32_t r) {
+  cur.mx = true;
 #pragma unroll
   for (int a = 0; a < NA; ++a) {
-    b.q[a] = ldg_stream(qp[a] + (size_t)s * 32);
-    b.s[a] = ldg_u8(sp[a] + (size_t)s * 2);
+    cur.row[a] = item_row_codes(p, c, gateup, cur.item, r, a, &cur.sw[a]);
+    cur.mx = cur.mx && cur.row[a] != nullptr;
   }
 }
 
-// Dequantize one slice from registers into its stage and signal it.
-template <int NA>
-__device__ __forceinline__ bool mx_slice(const PfCtx& c, int gs, uint32_t r, uint32_t c0, const MxBuf<NA>& b,
-                                         const int (&sig)[NA]) {
-  if (!pf_claim(c, gs)) return false;
-  const int st = gs % c.stages;
-  uint8_t* base = c.smem + (size_t)st * c.stage_bytes;
+template <int NA, int R>
+__device__ __forceinline__ void cursor_issue(PfCursor<NA>& cur, const ExpertParams& p, const PfCtx& c, bool gateup,
+                                             uint32_t r, int half, int g) {
+  const int tid = threadIdx.x;
+  uint8_t* slot = c.raw + (size_t)(g % R) * PfRaw<NA>::kStage;
+  if (cur.item < c.n_items) {
+    const int ns = c.nslices;
+    const int rowbytes = c.K / 2;
+    const int pa = prefetch_matrix<NA>(half);
+    if (cur.mx) {
+      if (pa >= 0 && (cur.s & 7) == 0) {
+        const int off = (cur.s + 8) * 32;
+        if (off < rowbytes) prefetch_l2(cur.row[pa] + off, (uint32_t)min(kPfL2Window, rowbytes - off));
+      }
 #pragma unroll
-  for (int a = 0; a < NA; ++a) dq_mx_block(base + a * kPfTileBytes, r, c0, b.q[a], b.s[a], sig[a]);
-  fence_async_smem();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&c.sh->full[st]);
-  return true;
+      for (int a = 0; a < NA; ++a) {
+        cp_async16(slot + a * (kPfDqWarps * 32 * 16) + tid * 16, cur.row[a] + (size_t)cur.s * 32 + half * 16);
+        cp_async4(slot + PfRaw<NA>::kQ + a * (kPfDqWarps * 32 * 4) + tid * 4, cur.sw[a] + (cur.s >> 1) * 4);
+      }
+    }
+    if (pa >= 0 && cur.s == (ns > 16 ? ns - 16 : 0)) {
+      const uint8_t* nq = item_row_codes(p, c, gateup, cur.item + gridDim.x, r, pa, nullptr);
+      if (nq) prefetch_l2(nq, (uint32_t)min(512, rowbytes));
+    }
+    if (++cur.s == ns) {
+      cur.s = 0;
+      cur.item += gridDim.x;
+      cursor_enter(cur, p, c, gateup, r);
+    }
+  }
+  cp_async_commit();
 }
 
 // Dequant warps: thread (row r, half) produces MX block 2s + half of weight
-// row m0 + r for every slice s, for gate and up (GATEUP) or down.
+// row m0 + r for every slice s, for gate and up (GATEUP) or down.  Routed
+// MXFP4 rows come through the raw ring; the bf16 shared expert's rows are
+// loaded directly.
 template <bool GATEUP>
 __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
   constexpr int NA = GATEUP ? 2 : 1;
-  const uint32_t r = threadIdx.x >> 1;
-  const int half = threadIdx.x & 1;
+  constexpr int R = GATEUP ? kPfRawGateUp : kPfRawDown;
+  const int tid = threadIdx.x;
+  const uint32_t r = (uint32_t)tid >> 1;
+  const int half = tid & 1;
   const uint32_t c0 = (uint32_t)half * 4;
   const int ns = c.nslices;
-  int gbase = 0;
-  for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, gbase += ns) {
+  PfShared& sh = *c.sh;
+  PfCursor<NA> cur;
+  cur.item = blockIdx.x;
+  cur.s = 0;
+  cursor_enter(cur, p, c, GATEUP, r);
+  if (cur.mx && prefetch_matrix<NA>(half) >= 0)
+    prefetch_l2(cur.row[prefetch_matrix<NA>(half)], (uint32_t)min(512, c.K / 2));
+  for (int g = 0; g < R; ++g) cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, g);
+  int g = 0, ci = 0;
+  bool ok = true;
+  for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
-    const int row = it.m0 + (int)r;
-    bool ok = true;
+    // Row shifts of this item, published by the epilogue warps.
+    const int slot = ci % kPfSigRing;
+    if (!pf_warp_wait(c, &sh.sig_full[slot], (ci / kPfSigRing) & 1)) break;
+    int sig[NA];
+#pragma unroll
+    for (int a = 0; a < NA; ++a) sig[a] = sh.sig[slot][a][r];
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(&sh.sig_empty[slot]);
     if (!it.shared) {
-      const moe_expert ex = p.experts[it.e];
-      const bool valid = row < c.M && expert_ptrs_ok(ex);
-      if (!expert_ptrs_ok(ex) && threadIdx.x == 0) set_status(c.hdr, MOE_ERR_DEVICE_CHECK);
-      const moe_mx_mat mats[2] = {GATEUP ? ex.gate : ex.down, ex.up};
-      const uint8_t* qp[NA];
-      const uint8_t* sp[NA];
-      int sig[NA];
+      for (int s = 0; s < ns; ++s, ++g) {
+        cp_async_wait<R - 1>();
+        const uint8_t* rs = c.raw + (size_t)(g % R) * PfRaw<NA>::kStage;
+        uint4 q[NA];
+        uint32_t sc[NA];
+        const int byte = ((s & 1) << 1) | half;
 #pragma unroll
-      for (int a = 0; a < NA; ++a) {
-        qp[a] = valid ? mats[a].q + (size_t)row * (c.K / 2) + half * 16 : nullptr;
-        sp[a] = valid ? mats[a].s + (size_t)row * (c.K / 32) + half : nullptr;
-        int smax = valid ? row_smax_part(mats[a].s + (size_t)row * (c.K / 32), c.K / 128, half, 2) : -1;
-        smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 1));
-        sig[a] = sigma_from_smax(smax);
-      }
-      MxBuf<NA> b0, b1, b2;
+        for (int a = 0; a < NA; ++a) {
+          q[a] = lds128(rs + a * (kPfDqWarps * 32 * 16) + tid * 16);
+          sc[a] = (*reinterpret_cast<const uint32_t*>(rs + PfRaw<NA>::kQ + a * (kPfDqWarps * 32 * 4) + tid * 4) >>
+                   (8 * byte)) & 0xFFu;
+        }
+        if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
+          ok = false;
+          break;
+        }
+        uint8_t* base = c.smem_a + (size_t)(g % c.a_stages) * c.a_bytes;
 #pragma unroll
-      for (int a = 0; a < NA; ++a) {
-        b0.q[a] = b1.q[a] = b2.q[a] = make_uint4(0, 0, 0, 0);
-        b0.s[a] = b1.s[a] = b2.s[a] = 0;
-      }
-      if (valid) {
-        mx_load(b0, qp, sp, 0);
-        if (ns > 1) mx_load(b1, qp, sp, 1);
-      }
-      for (int s = 0; s < ns && ok; s += 3) {
-        if (valid && s + 2 < ns) mx_load(b2, qp, sp, s + 2);
-        ok = mx_slice(c, gbase + s, r, c0, b0, sig);
-        if (!ok || s + 1 >= ns) break;
-        if (valid && s + 3 < ns) mx_load(b0, qp, sp, s + 3);
-        ok = mx_slice(c, gbase + s + 1, r, c0, b1, sig);
-        if (!ok || s + 2 >= ns) break;
-        if (valid && s + 4 < ns) mx_load(b1, qp, sp, s + 4);
-        ok = mx_slice(c, gbase + s + 2, r, c0, b2, sig);
+        for (int a = 0; a < NA; ++a) dq_mx_block(base + a * kPfTileBytes, r, c0, q[a], sc[a], sig[a]);
+        fence_async_smem();
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&sh.a_full[g % c.a_stages]);
+        cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, g + R);
       }
     } else {
       // bf16 shared expert: 32 weights (64 bytes) per thread and slice.
       const uint16_t* wp[NA];
       float scale[NA];
+      const int row = it.m0 + (int)r;
       const int rowc = row < c.M ? row : c.M - 1;
 #pragma unroll
       for (int a = 0; a < NA; ++a) {
         const uint16_t* base = GATEUP ? (a == 0 ? p.sh_gate : p.sh_up) : p.sh_down;
-        const int sidx = GATEUP ? a * p.I + rowc : 2 * p.I + rowc;
         wp[a] = base + (size_t)rowc * c.K + half * 32;
-        scale[a] = __int_as_float((__ldg(&p.ws.shsig[sidx]) + 127) << 23);
+        scale[a] = __int_as_float((sig[a] + 127) << 23);
       }
-      uint4 cur[NA][4];
-#pragma unroll
-      for (int a = 0; a < NA; ++a)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) cur[a][j] = ldg_stream(wp[a] + j * 8);
-      for (int s = 0; s < ns; ++s) {
-        uint4 nxt[NA][4];
-        const int sn = s + 1 < ns ? s + 1 : s;
+      for (int s = 0; s < ns; ++s, ++g) {
+        cp_async_wait<R - 1>();  // this slice's (empty) group
+        uint4 w[NA][4];
 #pragma unroll
         for (int a = 0; a < NA; ++a)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) nxt[a][j] = ldg_stream(wp[a] + (size_t)sn * kPfSliceK + j * 8);
-        ok = pf_claim(c, gbase + s);
-        if (!ok) break;
-        const int st = (gbase + s) % c.stages;
-        uint8_t* base = c.smem + (size_t)st * c.stage_bytes;
+          for (int j = 0; j < 4; ++j) w[a][j] = ldg_stream(wp[a] + (size_t)s * kPfSliceK + j * 8);
+        if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
+          ok = false;
+          break;
+        }
+        uint8_t* base = c.smem_a + (size_t)(g % c.a_stages) * c.a_bytes;
 #pragma unroll
-        for (int a = 0; a < NA; ++a) dq_bf16_block(base + a * kPfTileBytes, r, c0, cur[a], scale[a]);
+        for (int a = 0; a < NA; ++a) dq_bf16_block(base + a * kPfTileBytes, r, c0, w[a], scale[a]);
         fence_async_smem();
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(&c.sh->full[st]);
-#pragma unroll
-        for (int a = 0; a < NA; ++a)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) cur[a][j] = nxt[a][j];
+        if ((tid & 31) == 0) mbar_arrive(&sh.a_full[g % c.a_stages]);
+        cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, g + R);
       }
     }
-    if (!ok || *(volatile int*)&c.sh->abort_flag) break;
+    if (*(volatile int*)&sh.abort_flag) ok = false;
   }
+  cp_async_wait<0>();
 }
 
 // Loader warps: the item's token rows of the B operand (f16 activations for
@@ -416,7 +498,6 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
 // groups later, so several slices are in flight per thread.
 template <bool GATEUP>
 __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
-  constexpr int NA = GATEUP ? 2 : 1;
   const int l = threadIdx.x - kPfDqWarps * 32;  // 0..127
   const int lane = threadIdx.x & 31;
   const int ns = c.nslices;
@@ -454,11 +535,11 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
     }
     for (int s = 0; s < ns; ++s) {
       const int gs = gbase + s;
-      if (!pf_claim(c, gs)) {
+      if (!pf_claim(c, c.sh->b_empty, c.b_stages, gs)) {
         ok = false;
         break;
       }
-      uint8_t* btile = c.smem + (size_t)(gs % c.stages) * c.stage_bytes + NA * kPfTileBytes;
+      uint8_t* btile = c.smem_b + (size_t)(gs % c.b_stages) * kPfTileBytes;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (!use_chunk[j]) continue;
@@ -473,7 +554,7 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
         cp_async_wait<kPfBDepth - 1>();
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.sh->full[(pending - kPfBDepth) % c.stages]);
+        if (lane == 0) mbar_arrive(&c.sh->b_full[(pending - kPfBDepth) % c.b_stages]);
       }
     }
     if (*(volatile int*)&c.sh->abort_flag) ok = false;
@@ -484,39 +565,72 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
   __syncwarp();
   if (ok && lane == 0)
     for (int g = pending - (kPfBDepth - 1) > 0 ? pending - (kPfBDepth - 1) : 0; g < pending; ++g)
-      mbar_arrive(&c.sh->full[g % c.stages]);
+      mbar_arrive(&c.sh->b_full[g % c.b_stages]);
+}
+
+// Row shifts of local item j (the CTA's j-th item) into the shift ring, by
+// the epilogue warps (thread = one weight row).  Routed rows: from the E8M0
+// scales (sigma = 140 - max scale); shared-expert rows: from the pre-pass.
+template <bool GATEUP>
+__device__ __forceinline__ bool pf_publish_sig(const ExpertParams& p, const PfCtx& c, int j) {
+  PfShared& sh = *c.sh;
+  const int slot = j % kPfSigRing, use = j / kPfSigRing;
+  if (use > 0 && !pf_warp_wait(c, &sh.sig_empty[slot], (use - 1) & 1)) return false;
+  const int item = blockIdx.x + j * gridDim.x;
+  const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
+  const int rl = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
+  const int row = it.m0 + rl;
+  int s0 = 0, s1 = 0;
+  if (row < c.M) {
+    if (!it.shared) {
+      const moe_expert ex = p.experts[it.e];
+      if (expert_ptrs_ok(ex)) {
+        s0 = sigma_from_smax(row_smax_part((GATEUP ? ex.gate.s : ex.down.s) + (size_t)row * (c.K / 32), c.K / 128, 0, 1));
+        if (GATEUP) s1 = sigma_from_smax(row_smax_part(ex.up.s + (size_t)row * (c.K / 32), c.K / 128, 0, 1));
+      }
+    } else {
+      s0 = __ldg(&p.ws.shsig[GATEUP ? row : 2 * p.I + row]);
+      if (GATEUP) s1 = __ldg(&p.ws.shsig[p.I + row]);
+    }
+  }
+  sh.sig[slot][0][rl] = s0;
+  sh.sig[slot][1][rl] = s1;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.sig_full[slot]);
+  return true;
 }
 
 // Epilogue warps: warp q (= warp % 4) reads TMEM lanes 32q..32q+31, i.e.
 // weight rows m0 + 32q + lane, one fp32 column per token.
 //   gate/up: h[hpos0 + n][row] = f16(silu(g) * u), shifts removed;
 //   down:    out[token(n)][row] += weight(n) * y.
+// Before each item they publish the row shifts of the item kPfSigRing - 1
+// places ahead, so the dequant warps never wait on the scale reads.
 template <bool GATEUP>
 __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem) {
   const int q = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
   const int npairs = p.T * p.k;
   PfShared& sh = *c.sh;
+  const int n_local = blockIdx.x < c.n_items ? (c.n_items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  int published = 0;
   int ci = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
+    bool ok = true;
+    while (ok && published < n_local && published < ci + kPfSigRing) ok = pf_publish_sig<GATEUP>(p, c, published++);
+    if (!ok) break;
     const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
     const int b = ci & 1;
-    const int row = it.m0 + q * 32 + lane;
+    const int rl = q * 32 + lane;
+    const int row = it.m0 + rl;
     bool valid = row < c.M;
-    float rs0 = 1.f, rs1 = 1.f;  // 2^-sigma of the row: gate (or down), up
-    if (!it.shared) {
-      const moe_expert ex = p.experts[it.e];
-      valid = valid && expert_ptrs_ok(ex);
-      if (valid) {
-        const uint8_t* s0 = (GATEUP ? ex.gate.s : ex.down.s) + (size_t)row * (c.K / 32);
-        rs0 = ldexpf(1.f, -sigma_from_smax(row_smax_part(s0, c.K / 128, 0, 1)));
-        if (GATEUP)
-          rs1 = ldexpf(1.f, -sigma_from_smax(row_smax_part(ex.up.s + (size_t)row * (c.K / 32), c.K / 128, 0, 1)));
-      }
-    } else if (valid) {
-      rs0 = ldexpf(1.f, -__ldg(&p.ws.shsig[GATEUP ? row : 2 * p.I + row]));
-      if (GATEUP) rs1 = ldexpf(1.f, -__ldg(&p.ws.shsig[p.I + row]));
-    }
+    if (!it.shared) valid = valid && expert_ptrs_ok(p.experts[it.e]);
+    const int slot = ci % kPfSigRing;
+    if (!pf_warp_wait(c, &sh.sig_full[slot], (ci / kPfSigRing) & 1)) break;
+    const float rs0 = ldexpf(1.f, -sh.sig[slot][0][rl]);  // 2^-sigma of the row: gate (or down), up
+    const float rs1 = ldexpf(1.f, -sh.sig[slot][1][rl]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.sig_empty[slot]);
     // Per-column token and factor.  Each warp builds its own copy: a barrier
     // across the epilogue warps could not be left by a warp that aborts.
     float* col_scale = sh.col_scale[q];
@@ -601,14 +715,15 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
     bool ok = true;
     for (int s = 0; s < ns; ++s) {
       const int gs = ci * ns + s;
-      const int st = gs % c.stages, use = gs / c.stages;
-      if (!pf_wait(sh, &sh.full[st], use & 1, c.hdr)) {
+      const int sa = gs % c.a_stages, sb = gs % c.b_stages;
+      if (!pf_wait(sh, &sh.a_full[sa], (gs / c.a_stages) & 1, c.hdr) ||
+          !pf_wait(sh, &sh.b_full[sb], (gs / c.b_stages) & 1, c.hdr)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t abase = smem_u32(c.smem + (size_t)st * c.stage_bytes);
-      const uint32_t bbase = abase + NA * kPfTileBytes;
+      const uint32_t abase = smem_u32(c.smem_a + (size_t)sa * c.a_bytes);
+      const uint32_t bbase = smem_u32(c.smem_b + (size_t)sb * kPfTileBytes);
 #pragma unroll
       for (int kk = 0; kk < kPfSliceK / 16; ++kk) {
         const uint64_t bdesc = sdesc_sw128(bbase + kk * 32);
@@ -617,7 +732,8 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
           umma_f16(dcol + (uint32_t)(a * 128), sdesc_sw128(abase + a * kPfTileBytes + kk * 32), bdesc, idesc,
                    (s | kk) != 0 ? 1u : 0u);
       }
-      umma_commit(&sh.empty[st]);
+      umma_commit(&sh.a_empty[sa]);
+      umma_commit(&sh.b_empty[sb]);
     }
     umma_commit(&sh.accf[b]);
     if (!ok) {
@@ -635,8 +751,10 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
 // Persistent grouped GEMM, one CTA per SM.  GATEUP: A = gate and up rows (M =
 // I), K = H, B = f16 activations; else A = down rows (M = H), K = I, B = h.
 template <bool GATEUP>
-__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, int stages) {
+__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
   constexpr int NA = GATEUP ? 2 : 1;
+  constexpr int AS = GATEUP ? kPfAStagesGateUp : kPfAStagesDown;
+  constexpr int BS = GATEUP ? kPfBStagesGateUp : kPfBStagesDown;
   extern __shared__ uint8_t pf_dyn[];
   __shared__ PfShared sh;
   const int warp = threadIdx.x >> 5;
@@ -645,13 +763,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, int s
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(&sh.full[s], kPfDqWarps + kPfLdWarps);
-      mbar_init(&sh.empty[s], 1);
+    for (int s = 0; s < AS; ++s) {
+      mbar_init(&sh.a_full[s], kPfDqWarps);
+      mbar_init(&sh.a_empty[s], 1);
+    }
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(&sh.b_full[s], kPfLdWarps);
+      mbar_init(&sh.b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.accf[b], 1);
       mbar_init(&sh.acce[b], kPfEpWarps);
+    }
+    for (int i = 0; i < kPfSigRing; ++i) {
+      mbar_init(&sh.sig_full[i], kPfEpWarps);
+      mbar_init(&sh.sig_empty[i], kPfDqWarps + kPfEpWarps);
     }
     sh.abort_flag = 0;
     mbar_init_fence();
@@ -663,9 +789,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, int s
 
   PfCtx c;
   c.sh = &sh;
-  c.smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_dyn) + 1023) & ~(uintptr_t)1023);
-  c.stages = stages;
-  c.stage_bytes = (NA + 1) * kPfTileBytes;
+  c.smem_a = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_dyn) + 1023) & ~(uintptr_t)1023);
+  c.a_stages = AS;
+  c.b_stages = BS;
+  c.a_bytes = NA * kPfTileBytes;
+  c.smem_b = c.smem_a + (size_t)AS * c.a_bytes;
+  c.raw = c.smem_b + (size_t)BS * kPfTileBytes;
   c.K = GATEUP ? p.H : p.I;
   c.M = GATEUP ? p.I : p.H;
   c.nslices = c.K / kPfSliceK;
@@ -711,17 +840,19 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   if (!p.accumulate) {
     if ((err = cudaMemsetAsync(p.out, 0, (size_t)p.T * p.H * sizeof(float), s)) != cudaSuccess) return err;
   }
-  const int gu_stages = 4, dn_stages = 6;
-  const size_t gu_smem = (size_t)gu_stages * 3 * kPfTileBytes + 1024;
-  const size_t dn_smem = (size_t)dn_stages * 2 * kPfTileBytes + 1024;
+  // Weight tile ring + token tile ring + raw MXFP4 ring + alignment slack.
+  const size_t gu_smem = (size_t)(kPfAStagesGateUp * 2 + kPfBStagesGateUp) * kPfTileBytes +
+                         (size_t)kPfRawGateUp * PfRaw<2>::kStage + 1024;
+  const size_t dn_smem = (size_t)(kPfAStagesDown + kPfBStagesDown) * kPfTileBytes +
+                         (size_t)kPfRawDown * PfRaw<1>::kStage + 1024;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
   prof_before(MOE_STAGE_PF_GATEUP, s);
-  k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(p, gu_stages);
+  k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(p);
   prof_after(MOE_STAGE_PF_GATEUP, s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   prof_before(MOE_STAGE_PF_DOWN, s);
-  k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(p, dn_stages);
+  k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(p);
   prof_after(MOE_STAGE_PF_DOWN, s);
   return cudaGetLastError();
 }
