@@ -167,6 +167,38 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
                 int accumulate, int32_t* ids_out, float* w_out, int path, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* Size of the library's own static device scratch (see below). */
+#define MOE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* moe_forward for callers that cannot provide a workspace: the same launch
+ * sequence and results as moe_forward, but the workspace is a fixed
+ * MOE_STATIC_SCRATCH_BYTES region of device memory that the library itself
+ * declares (one per device), so the call allocates nothing and needs no
+ * `ws` argument.  This entry point has no counterpart on the pages; it exists
+ * for host programs that hold only the layer's own buffers and have no
+ * device allocator to hand the library (or must not allocate while serving).
+ *   - Limit: shapes with moe_workspace_bytes(shape) > MOE_STATIC_SCRATCH_BYTES
+ *     are rejected with MOE_ERR_WORKSPACE before anything is launched (the
+ *     pages' layer shape H = 7168, E = 896, k = 16, I = 1408 fits up to T = 14).
+ *   - Set-up: the first call on a device (that device current) looks up the
+ *     scratch address once; a CUDA failure there returns MOE_ERR_CUDA.  If the
+ *     caller records its work into a CUDA graph, make one call before
+ *     recording so that this set-up is not part of the recorded work.
+ *   - Contents: the scratch needs no initialisation; every call resets what it
+ *     relies on (the status word and the counters) at its start.
+ *   - Concurrency: all calls on one device share the one scratch region.  Two
+ *     calls that may overlap in time (different streams, or host threads
+ *     without ordering between them) race on it and give undefined results;
+ *     order them (one stream, or events).
+ *   - status_dev: a DEVICE int32 that receives the call's device status word
+ *     (what moe_device_status reports for an explicit workspace), copied on
+ *     `stream` after the layer; NULL to skip.
+ * Other arguments as for moe_forward. */
+int moe_forward_static_scratch(const moe_shape* shape, const void* x, int x_dtype, const float* w_router,
+                               const float* b_router, const moe_expert* experts, const moe_dense_bf16* shared,
+                               float* out, int accumulate, int32_t* ids_out, float* w_out, int path,
+                               int32_t* status_dev, void* stream);
+
 /* Synchronises `stream`, then reads the device status word of `ws` into
  * *status_out (MOE_OK if no kernel flagged a problem since the last call that
  * began with this workspace).  Returns MOE_ERR_CUDA if the synchronisation or

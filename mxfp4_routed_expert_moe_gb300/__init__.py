@@ -34,7 +34,8 @@ DECODE_MAX_T = 64
 
 # Every symbol the header declares (checked by the tests against the .so).
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_route", "moe_mxfp4_experts",
-           "moe_forward", "moe_device_status", "moe_profile_events")
+           "moe_forward", "moe_device_status", "moe_profile_events", "moe_forward_static_scratch")
+STATIC_SCRATCH_BYTES = 8 << 20
 
 STAGE_ROUTE, STAGE_GATEUP, STAGE_DOWN, STAGE_COMBINE, STAGE_PF_GATEUP, STAGE_PF_DOWN = 1, 2, 3, 4, 5, 6
 
@@ -79,6 +80,8 @@ def lib():
             L.moe_forward.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp, i32, vp, sz, vp]
             L.moe_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
             L.moe_profile_events.argtypes = [i32, vp, vp]
+            L.moe_forward_static_scratch.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp,
+                                                     i32, vp, vp]
             _LIB = L
     return _LIB
 
@@ -159,6 +162,22 @@ def forward(shp: Shape, x, w_router, b_router, experts, shared, out, accumulate,
                            _ptr(experts), sh, _ptr(out), int(bool(accumulate)), _ptr(ids_out), _ptr(w_out),
                            int(path), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "moe_forward")
+
+
+def forward_static_scratch(shp: Shape, x, w_router, b_router, experts, shared, out, accumulate, ids_out=None,
+                           w_out=None, path=PATH_AUTO, status_dev=None, stream=None):
+    """moe_forward_static_scratch: the layer with the library's own static
+    device scratch as workspace (no workspace argument; nothing allocated).
+    For callers that cannot hand the library device memory; calls on one
+    device must not overlap in time.  ``status_dev`` is None or a device int32
+    tensor that receives the call's device status word."""
+    sh = None
+    if shared is not None:
+        sh = ctypes.byref(DenseBf16(_ptr(shared[0]), _ptr(shared[1]), _ptr(shared[2])))
+    rc = lib().moe_forward_static_scratch(ctypes.byref(shp), _ptr(x), _dtype_of(x), _ptr(w_router), _ptr(b_router),
+                                          _ptr(experts), sh, _ptr(out), int(bool(accumulate)), _ptr(ids_out),
+                                          _ptr(w_out), int(path), _ptr(status_dev), _stream(stream))
+    _check(rc, "moe_forward_static_scratch")
 
 
 def profile_events(stage: int, before=None, after=None) -> None:

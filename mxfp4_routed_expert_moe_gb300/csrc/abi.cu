@@ -3,6 +3,8 @@
 // synchronises except moe_device_status().
 #include <string.h>
 
+#include <mutex>
+
 #include "kernels.h"
 
 using namespace moe;
@@ -134,6 +136,28 @@ int run_experts(const ExpertParams& p, int path, cudaStream_t st) {
   return cuda_status(launch_prefill_experts(p, st));
 }
 
+// Workspace of moe_forward_static_scratch: a fixed region in the library's own
+// device memory (one instance per device), so that call allocates nothing.
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (with that device current).
+int static_scratch_ptr(void** out) {
+  constexpr int kMaxDevices = 64;
+  static void* table[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!table[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    table[dev] = p;
+  }
+  *out = table[dev];
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -232,6 +256,26 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
   }
   if ((st = do_route(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L, false, s)) != MOE_OK) return st;
   return run_experts(p, rpath, s);
+}
+
+int moe_forward_static_scratch(const moe_shape* shape, const void* x, int x_dtype, const float* w_router,
+                               const float* b_router, const moe_expert* experts, const moe_dense_bf16* shared,
+                               float* out, int accumulate, int32_t* ids_out, float* w_out, int path,
+                               int32_t* status_dev, void* stream) {
+  int st = validate_shape(shape);
+  if (st != MOE_OK) return st;
+  if (ws_layout(*shape, nullptr).total > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  if (status_dev && !aligned(status_dev, 4)) return MOE_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if ((st = static_scratch_ptr(&scratch)) != MOE_OK) return st;
+  st = moe_forward(shape, x, x_dtype, w_router, b_router, experts, shared, out, accumulate, ids_out, w_out, path,
+                   scratch, MOE_STATIC_SCRATCH_BYTES, stream);
+  if (st != MOE_OK) return st;
+  if (status_dev &&
+      cudaMemcpyAsync(status_dev, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, (cudaStream_t)stream) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 int moe_profile_events(int stage, void* before, void* after) {
