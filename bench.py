@@ -55,6 +55,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """The slowest rank's time: every replica ran the same work, so the job
+    took as long as its slowest member."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_replica: int, ms: float) -> float:
+    """Whole-job throughput of `world` replicas, each processing
+    `tokens_per_replica` tokens per step of `ms` milliseconds (weak scaling)."""
+    return world * tokens_per_replica / (ms / 1000.0)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -492,12 +509,8 @@ def main():
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * wl.T / (ms / 1000.0)
+    ms = max_over_ranks(statistics.mean(step_ms), world, device)
+    value = job_tokens_per_s(world, wl.T, ms)
 
     hbm, bf16, bf16_sus, peak_src = peaks()
     stage = layer.dominant_stage()
@@ -538,7 +551,7 @@ def main():
         "stage_ms": breakdown,
         "roofline": roof,
         "clocks": clk,
-        "e2e": {"value": world * wl.T / (e2e_ms / 1000.0), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, wl.T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": layer.x.numel() * layer.x.element_size(),
                 "d2h_bytes_per_step": layer.out.numel() * 4, "ms_per_step": e2e_ms},
         "gpu_launches": layer.launches_per_step() * args.steps,
