@@ -35,29 +35,38 @@ namespace moe {
 
 constexpr int kPfSliceK = 64;            // contraction elements per stage (one 128-byte swizzle row)
 constexpr int kPfTileBytes = 128 * 128;  // one 128-row x 64-element f16 tile
-constexpr int kPfDqWarps = 8;            // warps 0-7: weight dequant (2 threads per weight row)
-constexpr int kPfLdWarps = 4;            // warps 8-11: token rows (cp.async)
-constexpr int kPfEpWarps = 4;            // warps 12-15: epilogue (warp % 4 = TMEM lane quarter)
-constexpr int kPfMmaWarp = kPfDqWarps + kPfLdWarps + kPfEpWarps;  // warp 16: TMEM owner, MMA issuer
-constexpr int kPfThreads = (kPfMmaWarp + 1) * 32;
-constexpr int kPfBDepth = 4;             // cp.async groups in flight per loader thread
+// Weight dequant: two groups of 8 warps; group k converts the slices of parity
+// k (2 threads per weight row in each group), so each warp's per-slice chain
+// of waits, conversion and signalling overlaps the other group's.
+constexpr int kPfDqGroups = 2;
+constexpr int kPfDqGroupWarps = 8;
+constexpr int kPfDqGroupThreads = kPfDqGroupWarps * 32;
+constexpr int kPfDqWarps = kPfDqGroups * kPfDqGroupWarps;  // warps 0-15
+constexpr int kPfLdWarps = 4;            // warps 16-19: token rows (cp.async)
+constexpr int kPfEpWarps = 4;            // warps 20-23: epilogue (warp % 4 = TMEM lane quarter)
+// MMA issue: one thread issues a tcgen05.mma only every ~100 cycles whatever
+// its size, so the gate/up kernel issues from two warps, one accumulator each
+// (gate, up).  The down kernel has one accumulator and one issuer.
+constexpr int kPfMmaWarp = kPfDqWarps + kPfLdWarps + kPfEpWarps;  // warps 24-25: MMA issuers; 24 owns TMEM
+constexpr int kPfMmaWarps = 2;
+constexpr int kPfThreads = (kPfMmaWarp + kPfMmaWarps) * 32;
 constexpr int kPfMaxStages = 8;
 // Rings (per kernel): f16 weight tiles from the dequant warps (A), f16 token
 // rows from the loader warps (B), raw MXFP4 bytes of the dequant threads.
-constexpr int kPfAStagesGateUp = 2, kPfBStagesGateUp = 5;
+constexpr int kPfAStagesGateUp = 3, kPfBStagesGateUp = 5;
 constexpr int kPfAStagesDown = 3, kPfBStagesDown = 6;
 constexpr int kPfL2Window = 256;         // bytes of each weight row prefetched into L2 at a time
 constexpr uint32_t kPfTmemCols = 512;    // 2 accumulator buffers x (gate 128 + up 128) columns
 constexpr int kPfSigRing = 4;            // items whose row shifts are published ahead
-// Raw MXFP4 ring of the dequant threads: per slice and thread 16 bytes of
-// codes and the 4-byte scale word per matrix, cp.async'd this many slices
-// ahead (about 48 KB in flight per SM for either kernel).
-constexpr int kPfRawGateUp = 6;
-constexpr int kPfRawDown = 12;
+// Raw MXFP4 ring of each dequant group: per slice and thread 16 bytes of
+// codes and the 4-byte scale word per matrix, cp.async'd this many of the
+// group's slices ahead (about 48 KB in flight per SM for either kernel).
+constexpr int kPfRawGateUp = 2;
+constexpr int kPfRawDown = 6;
 template <int NA>
 struct PfRaw {
-  static constexpr int kQ = NA * kPfDqWarps * 32 * 16;   // codes
-  static constexpr int kStage = kQ + NA * kPfDqWarps * 32 * 4;  // + scale words
+  static constexpr int kQ = NA * kPfDqGroupThreads * 16;              // codes
+  static constexpr int kStage = kQ + NA * kPfDqGroupThreads * 4;      // + scale words
 };
 static_assert(kPfEpWarps == 4 && (kPfDqWarps + kPfLdWarps) % 4 == 0, "epilogue warps must cover lane quarters 0-3");
 
@@ -248,14 +257,14 @@ __device__ __forceinline__ void dq_bf16_block(uint8_t* tile, uint32_t r, uint32_
 
 // -------------------------------------------------------- CTA control --
 struct PfShared {
-  uint64_t a_full[kPfMaxStages];   // weight tile stage filled: 8 dequant warps
+  uint64_t a_full[kPfMaxStages];   // weight tile stage filled: the 8 warps of one dequant group
   uint64_t a_empty[kPfMaxStages];  // ... consumed: tcgen05.commit
-  uint64_t b_full[kPfMaxStages];   // token tile stage filled: 4 loader warps
+  uint64_t b_full[kPfMaxStages];   // token tile stage filled: 128 loader threads (cp.async arrivals)
   uint64_t b_empty[kPfMaxStages];  // ... consumed: tcgen05.commit
-  uint64_t accf[2];              // accumulator buffer ready: tcgen05.commit
+  uint64_t accf[2];              // accumulator buffer ready: tcgen05.commit of each issuer
   uint64_t acce[2];              // accumulator buffer drained: 4 epilogue warps
   uint64_t sig_full[kPfSigRing];  // row shifts of an item published: 4 epilogue warps
-  uint64_t sig_empty[kPfSigRing]; // ... and read: 8 dequant + 4 epilogue warps
+  uint64_t sig_empty[kPfSigRing]; // ... and read: 16 dequant + 4 epilogue warps
   uint32_t tmem_base;
   int abort_flag;
   int sig[kPfSigRing][2][kPfMTile];       // row shifts (gate/down, up) of upcoming items
@@ -363,11 +372,13 @@ __device__ __forceinline__ void cursor_enter(PfCursor<NA>& cur, const ExpertPara
   }
 }
 
+// Issue the cursor's slice into slot j % R of the group's raw ring, then move
+// the cursor kPfDqGroups slices on (the group's next slice).
 template <int NA, int R>
 __device__ __forceinline__ void cursor_issue(PfCursor<NA>& cur, const ExpertParams& p, const PfCtx& c, bool gateup,
-                                             uint32_t r, int half, int g) {
-  const int tid = threadIdx.x;
-  uint8_t* slot = c.raw + (size_t)(g % R) * PfRaw<NA>::kStage;
+                                             uint32_t r, int half, uint8_t* raw, int j) {
+  const int tid = threadIdx.x % kPfDqGroupThreads;
+  uint8_t* slot = raw + (size_t)(j % R) * PfRaw<NA>::kStage;
   if (cur.item < c.n_items) {
     const int ns = c.nslices;
     const int rowbytes = c.K / 2;
@@ -379,16 +390,17 @@ __device__ __forceinline__ void cursor_issue(PfCursor<NA>& cur, const ExpertPara
       }
 #pragma unroll
       for (int a = 0; a < NA; ++a) {
-        cp_async16(slot + a * (kPfDqWarps * 32 * 16) + tid * 16, cur.row[a] + (size_t)cur.s * 32 + half * 16);
-        cp_async4(slot + PfRaw<NA>::kQ + a * (kPfDqWarps * 32 * 4) + tid * 4, cur.sw[a] + (cur.s >> 1) * 4);
+        cp_async16(slot + a * (kPfDqGroupThreads * 16) + tid * 16, cur.row[a] + (size_t)cur.s * 32 + half * 16);
+        cp_async4(slot + PfRaw<NA>::kQ + a * (kPfDqGroupThreads * 4) + tid * 4, cur.sw[a] + (cur.s >> 1) * 4);
       }
     }
     if (pa >= 0 && cur.s == (ns > 16 ? ns - 16 : 0)) {
       const uint8_t* nq = item_row_codes(p, c, gateup, cur.item + gridDim.x, r, pa, nullptr);
       if (nq) prefetch_l2(nq, (uint32_t)min(512, rowbytes));
     }
-    if (++cur.s == ns) {
-      cur.s = 0;
+    cur.s += kPfDqGroups;
+    if (cur.s >= ns) {
+      cur.s -= ns;
       cur.item += gridDim.x;
       cursor_enter(cur, p, c, gateup, r);
     }
@@ -396,28 +408,32 @@ __device__ __forceinline__ void cursor_issue(PfCursor<NA>& cur, const ExpertPara
   cp_async_commit();
 }
 
-// Dequant warps: thread (row r, half) produces MX block 2s + half of weight
-// row m0 + r for every slice s, for gate and up (GATEUP) or down.  Routed
-// MXFP4 rows come through the raw ring; the bf16 shared expert's rows are
-// loaded directly.
+// Dequant warps: group k (warps 8k .. 8k+7) converts the slices s of every
+// item with s % 2 == k; in a group, thread (row r, half) produces MX block
+// 2s + half of weight row m0 + r, for gate and up (GATEUP) or down.  Routed
+// MXFP4 rows come through the group's raw ring; the bf16 shared expert's rows
+// are loaded directly.  (The slice count per item, K / 64, is even.)
 template <bool GATEUP>
 __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
   constexpr int NA = GATEUP ? 2 : 1;
   constexpr int R = GATEUP ? kPfRawGateUp : kPfRawDown;
-  const int tid = threadIdx.x;
+  const int grp = threadIdx.x / kPfDqGroupThreads;
+  const int tid = threadIdx.x % kPfDqGroupThreads;
+  const int lane = threadIdx.x & 31;
   const uint32_t r = (uint32_t)tid >> 1;
   const int half = tid & 1;
   const uint32_t c0 = (uint32_t)half * 4;
   const int ns = c.nslices;
   PfShared& sh = *c.sh;
+  uint8_t* raw = c.raw + (size_t)grp * R * PfRaw<NA>::kStage;
   PfCursor<NA> cur;
   cur.item = blockIdx.x;
-  cur.s = 0;
+  cur.s = grp;
   cursor_enter(cur, p, c, GATEUP, r);
-  if (cur.mx && prefetch_matrix<NA>(half) >= 0)
+  if (grp == 0 && cur.mx && prefetch_matrix<NA>(half) >= 0)
     prefetch_l2(cur.row[prefetch_matrix<NA>(half)], (uint32_t)min(512, c.K / 2));
-  for (int g = 0; g < R; ++g) cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, g);
-  int g = 0, ci = 0;
+  for (int j = 0; j < R; ++j) cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, raw, j);
+  int j = 0, ci = 0;  // j: the group's slices consumed so far
   bool ok = true;
   for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
@@ -428,36 +444,10 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
 #pragma unroll
     for (int a = 0; a < NA; ++a) sig[a] = sh.sig[slot][a][r];
     __syncwarp();
-    if ((tid & 31) == 0) mbar_arrive(&sh.sig_empty[slot]);
-    if (!it.shared) {
-      for (int s = 0; s < ns; ++s, ++g) {
-        cp_async_wait<R - 1>();
-        const uint8_t* rs = c.raw + (size_t)(g % R) * PfRaw<NA>::kStage;
-        uint4 q[NA];
-        uint32_t sc[NA];
-        const int byte = ((s & 1) << 1) | half;
-#pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          q[a] = lds128(rs + a * (kPfDqWarps * 32 * 16) + tid * 16);
-          sc[a] = (*reinterpret_cast<const uint32_t*>(rs + PfRaw<NA>::kQ + a * (kPfDqWarps * 32 * 4) + tid * 4) >>
-                   (8 * byte)) & 0xFFu;
-        }
-        if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
-          ok = false;
-          break;
-        }
-        uint8_t* base = c.smem_a + (size_t)(g % c.a_stages) * c.a_bytes;
-#pragma unroll
-        for (int a = 0; a < NA; ++a) dq_mx_block(base + a * kPfTileBytes, r, c0, q[a], sc[a], sig[a]);
-        fence_async_smem();
-        __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(&sh.a_full[g % c.a_stages]);
-        cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, g + R);
-      }
-    } else {
-      // bf16 shared expert: 32 weights (64 bytes) per thread and slice.
-      const uint16_t* wp[NA];
-      float scale[NA];
+    if (lane == 0) mbar_arrive(&sh.sig_empty[slot]);
+    const uint16_t* wp[NA];
+    float scale[NA];
+    if (it.shared) {
       const int row = it.m0 + (int)r;
       const int rowc = row < c.M ? row : c.M - 1;
 #pragma unroll
@@ -466,25 +456,46 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
         wp[a] = base + (size_t)rowc * c.K + half * 32;
         scale[a] = __int_as_float((sig[a] + 127) << 23);
       }
-      for (int s = 0; s < ns; ++s, ++g) {
-        cp_async_wait<R - 1>();  // this slice's (empty) group
-        uint4 w[NA][4];
+    }
+    for (int s = grp; s < ns; s += kPfDqGroups, ++j) {
+      const int g = ci * ns + s;
+      cp_async_wait<R - 1>();  // this slice's group (empty for the shared expert)
+      uint8_t* base = c.smem_a + (size_t)(g % c.a_stages) * c.a_bytes;
+      if (!it.shared) {
+        const uint8_t* rs = raw + (size_t)(j % R) * PfRaw<NA>::kStage;
+        uint4 q[NA];
+        uint32_t sc[NA];
+        const int byte = ((s & 1) << 1) | half;
 #pragma unroll
-        for (int a = 0; a < NA; ++a)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) w[a][j] = ldg_stream(wp[a] + (size_t)s * kPfSliceK + j * 8);
+        for (int a = 0; a < NA; ++a) {
+          q[a] = lds128(rs + a * (kPfDqGroupThreads * 16) + tid * 16);
+          sc[a] = (*reinterpret_cast<const uint32_t*>(rs + PfRaw<NA>::kQ + a * (kPfDqGroupThreads * 4) + tid * 4) >>
+                   (8 * byte)) & 0xFFu;
+        }
         if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
           ok = false;
           break;
         }
-        uint8_t* base = c.smem_a + (size_t)(g % c.a_stages) * c.a_bytes;
+#pragma unroll
+        for (int a = 0; a < NA; ++a) dq_mx_block(base + a * kPfTileBytes, r, c0, q[a], sc[a], sig[a]);
+      } else {
+        // bf16 shared expert: 32 weights (64 bytes) per thread and slice.
+        uint4 w[NA][4];
+#pragma unroll
+        for (int a = 0; a < NA; ++a)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) w[a][jj] = ldg_stream(wp[a] + (size_t)s * kPfSliceK + jj * 8);
+        if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int a = 0; a < NA; ++a) dq_bf16_block(base + a * kPfTileBytes, r, c0, w[a], scale[a]);
-        fence_async_smem();
-        __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(&sh.a_full[g % c.a_stages]);
-        cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, g + R);
       }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.a_full[g % c.a_stages]);
+      cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, raw, j + R);
     }
     if (*(volatile int*)&sh.abort_flag) ok = false;
   }
@@ -493,16 +504,16 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
 
 // Loader warps: the item's token rows of the B operand (f16 activations for
 // gate/up, f16 h for down), 16-byte cp.async chunks into the SW128 layout;
-// rows between the token count and the next multiple of 16 are zero.  Each
-// slice is one cp.async group; a group's stage is signalled kPfBDepth - 1
-// groups later, so several slices are in flight per thread.
+// rows between the token count and the next multiple of 16 are zero-filled
+// by cp.async as well.  Each thread then arrives on the stage's barrier
+// through cp.async.mbarrier.arrive, which fires when its copies have landed,
+// so the loader never waits for its own copies: it runs ahead as far as the
+// ring allows and each stage is ready as soon as its data is.
 template <bool GATEUP>
 __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
   const int l = threadIdx.x - kPfDqWarps * 32;  // 0..127
-  const int lane = threadIdx.x & 31;
   const int ns = c.nslices;
   const int npairs = p.T * p.k;
-  int pending = 0;  // groups committed so far == global slices issued
   bool ok = true;
   int gbase = 0;
   for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x, gbase += ns) {
@@ -546,26 +557,13 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
         if (src[j])
           cp_async16(btile + dst[j], src[j] + (size_t)s * kPfSliceK);
         else
-          *reinterpret_cast<uint4*>(btile + dst[j]) = make_uint4(0, 0, 0, 0);
+          cp_async16_zfill(btile + dst[j], p.ws.xh, 0u);
       }
-      cp_async_commit();
-      ++pending;
-      if (pending >= kPfBDepth) {
-        cp_async_wait<kPfBDepth - 1>();
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.sh->b_full[(pending - kPfBDepth) % c.b_stages]);
-      }
+      cp_async_mbar_arrive(&c.sh->b_full[gs % c.b_stages]);
     }
     if (*(volatile int*)&c.sh->abort_flag) ok = false;
   }
-  // Complete and signal the groups still in flight.
-  cp_async_wait<0>();
-  fence_async_smem();
-  __syncwarp();
-  if (ok && lane == 0)
-    for (int g = pending - (kPfBDepth - 1) > 0 ? pending - (kPfBDepth - 1) : 0; g < pending; ++g)
-      mbar_arrive(&c.sh->b_full[g % c.b_stages]);
+  cp_async_wait_all();
 }
 
 // Row shifts of local item j (the CTA's j-th item) into the shift ring, by
@@ -654,24 +652,25 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
     if (!pf_warp_wait(c, &sh.accf[b], (ci >> 1) & 1)) break;
     tc_fence_after();
     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
-    for (int c0 = 0; c0 < it.cnt; c0 += 32) {
-      uint32_t g[32];
-      tmem_ld32(tbase + (uint32_t)c0, g);
+    for (int c0 = 0; c0 < it.cnt; c0 += 16) {
+      uint32_t g[16];
+      tmem_ld16(tbase + (uint32_t)c0, g);
       if (GATEUP) {
-        uint32_t u[32];
-        tmem_ld32(tbase + 128u + (uint32_t)c0, u);
+        uint32_t u[16];
+        tmem_ld16(tbase + 128u + (uint32_t)c0, u);
         tmem_ld_wait();
         if (valid) {
-          __half* hout = reinterpret_cast<__half*>(p.ws.h) + (size_t)(it.hpos0 + c0) * p.I + row;
+          __half* hout = reinterpret_cast<__half*>(p.ws.h);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (c0 + i < it.cnt) {
-              const float xs = col_scale[c0 + i];
-              const float gv = (__uint_as_float(g[i]) * rs0) * xs;
-              const float uv = (__uint_as_float(u[i]) * rs1) * xs;
+          for (int i = 0; i < 16; ++i) {
+            const int n = c0 + i;
+            if (n < it.cnt) {
+              const float xs = col_scale[n];
+              const float gv = __uint_as_float(g[i]) * rs0 * xs;
+              const float uv = __uint_as_float(u[i]) * rs1 * xs;
               const float hv = silu_f32(gv) * uv;
               if (fabsf(hv) > 65504.f) set_status(c.hdr, MOE_ERR_RANGE);
-              hout[(size_t)i * p.I] = __float2half_rn(hv);
+              hout[(size_t)(it.hpos0 + n) * p.I + row] = __float2half_rn(hv);
             }
           }
         }
@@ -679,10 +678,11 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (c0 + i < it.cnt) {
-              const float v = (__uint_as_float(g[i]) * rs0) * col_scale[c0 + i];
-              atomicAdd(&p.out[(size_t)col_tok[c0 + i] * p.H + row], v);
+          for (int i = 0; i < 16; ++i) {
+            const int n = c0 + i;
+            if (n < it.cnt) {
+              const float v = (__uint_as_float(g[i]) * rs0) * col_scale[n];
+              atomicAdd(&p.out[(size_t)col_tok[n] * p.H + row], v);
             }
           }
         }
@@ -694,13 +694,17 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
   }
 }
 
-// MMA warp, lane 0: per item, waits for a free accumulator buffer, then per
-// slice for a full stage, issues 4 (x2 for gate and up) K = 16 MMAs
-// M = 128 x N = round16(tokens), and releases the stage with tcgen05.commit;
-// the item's last commit marks the accumulator ready.
+// MMA issuers (lane 0 of warp 24, and of warp 25 in the gate/up kernel): per
+// item, wait for a free accumulator buffer, then per stage for the weight and
+// token tiles, issue 4 K = 16 MMAs M = 128 x N = round16(tokens) into
+// accumulator `which` (gate/up: matrix `which`; down: the one accumulator),
+// and release the stages with tcgen05.commit; each issuer's last commit of the
+// item counts towards the accumulator buffer being ready.  (Splitting the down
+// contraction into even and odd stages over two issuers gave wrong tiles and
+// a stalled wait in testing; it is not used.)
 template <bool GATEUP>
-__device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem) {
-  constexpr int NA = GATEUP ? 2 : 1;
+__device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem, int which) {
+  if (!GATEUP && which != 0) return;
   PfShared& sh = *c.sh;
   const int ns = c.nslices;
   int ci = 0;
@@ -711,8 +715,9 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
     tc_fence_after();
     const int nmma = (it.cnt + 15) & ~15;
     const uint32_t idesc = idesc_f16_f32(kPfMTile, nmma);
-    const uint32_t dcol = tmem + (uint32_t)(b * 256);
+    const uint32_t dcol = tmem + (uint32_t)(b * 256 + which * 128);
     bool ok = true;
+    bool first = true;
     for (int s = 0; s < ns; ++s) {
       const int gs = ci * ns + s;
       const int sa = gs % c.a_stages, sb = gs % c.b_stages;
@@ -721,16 +726,14 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
         ok = false;
         break;
       }
+      fence_async_smem();  // the token tile was written by cp.async (generic proxy)
       tc_fence_after();
-      const uint32_t abase = smem_u32(c.smem_a + (size_t)sa * c.a_bytes);
+      const uint32_t abase = smem_u32(c.smem_a + (size_t)sa * c.a_bytes + (GATEUP ? which * kPfTileBytes : 0));
       const uint32_t bbase = smem_u32(c.smem_b + (size_t)sb * kPfTileBytes);
 #pragma unroll
       for (int kk = 0; kk < kPfSliceK / 16; ++kk) {
-        const uint64_t bdesc = sdesc_sw128(bbase + kk * 32);
-#pragma unroll
-        for (int a = 0; a < NA; ++a)
-          umma_f16(dcol + (uint32_t)(a * 128), sdesc_sw128(abase + a * kPfTileBytes + kk * 32), bdesc, idesc,
-                   (s | kk) != 0 ? 1u : 0u);
+        umma_f16(dcol, sdesc_sw128(abase + kk * 32), sdesc_sw128(bbase + kk * 32), idesc, first ? 0u : 1u);
+        first = false;
       }
       umma_commit(&sh.a_empty[sa]);
       umma_commit(&sh.b_empty[sb]);
@@ -763,16 +766,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
+    // gate/up: both issuers read every stage; down: one issuer per stage.
     for (int s = 0; s < AS; ++s) {
-      mbar_init(&sh.a_full[s], kPfDqWarps);
-      mbar_init(&sh.a_empty[s], 1);
+      mbar_init(&sh.a_full[s], kPfDqGroupWarps);
+      mbar_init(&sh.a_empty[s], GATEUP ? kPfMmaWarps : 1);
     }
     for (int s = 0; s < BS; ++s) {
-      mbar_init(&sh.b_full[s], kPfLdWarps);
-      mbar_init(&sh.b_empty[s], 1);
+      mbar_init(&sh.b_full[s], kPfLdWarps * 32);
+      mbar_init(&sh.b_empty[s], GATEUP ? kPfMmaWarps : 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sh.accf[b], 1);
+      mbar_init(&sh.accf[b], GATEUP ? kPfMmaWarps : 1);
       mbar_init(&sh.acce[b], kPfEpWarps);
     }
     for (int i = 0; i < kPfSigRing; ++i) {
@@ -812,7 +816,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
   else if (warp < kPfMmaWarp)
     pf_epilogue_role<GATEUP>(p, c, tmem);
   else if ((threadIdx.x & 31) == 0)
-    pf_mma_role<GATEUP>(p, c, tmem);
+    pf_mma_role<GATEUP>(p, c, tmem, warp - kPfMmaWarp);
 
   tc_fence_before();
   __syncthreads();
@@ -842,9 +846,9 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   }
   // Weight tile ring + token tile ring + raw MXFP4 ring + alignment slack.
   const size_t gu_smem = (size_t)(kPfAStagesGateUp * 2 + kPfBStagesGateUp) * kPfTileBytes +
-                         (size_t)kPfRawGateUp * PfRaw<2>::kStage + 1024;
+                         (size_t)kPfDqGroups * kPfRawGateUp * PfRaw<2>::kStage + 1024;
   const size_t dn_smem = (size_t)(kPfAStagesDown + kPfBStagesDown) * kPfTileBytes +
-                         (size_t)kPfRawDown * PfRaw<1>::kStage + 1024;
+                         (size_t)kPfDqGroups * kPfRawDown * PfRaw<1>::kStage + 1024;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
   prof_before(MOE_STAGE_PF_GATEUP, s);
