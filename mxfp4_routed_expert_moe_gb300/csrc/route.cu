@@ -226,66 +226,114 @@ cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
 }
 
 // ------------------------------------------------------- prefill router GEMM --
-// s = x Wr^T (+ b) in fp32 on CUDA cores: 64x64 output tiles, 16-wide K steps,
-// 4x4 outputs per thread.  Also clears the per-expert token masks.
-constexpr int kGmTile = 64, kGmK = 16;
+// s = x Wr^T (+ b) in fp32 on CUDA cores.  A CTA computes 64 experts x 64
+// tokens; thread (tx, ty) of 16 x 16 holds 4 experts x 4 tokens.  Each
+// 16-wide K step is staged through double-buffered shared memory (vector
+// loads for the next step are in flight while this one is computed), summed
+// in fp32 and added into a double-float accumulator (hi, lo).  Also clears
+// the per-expert token masks.
+constexpr int kGmTT = 64, kGmTE = 64, kGmK = 16;
 
 template <bool XBF16>
 __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
-  __shared__ float xs[kGmK][kGmTile + 4];
-  __shared__ float ws_[kGmK][kGmTile + 4];
+  constexpr int TT = kGmTT, TE = kGmTE, KS = kGmK, NE = TE / 16, NW = TE * 4 / 256;
+  __shared__ __align__(16) float xs[2][KS][TT + 4];
+  __shared__ __align__(16) float ws_[2][KS][TE + 4];
   const int T = p.T, H = p.H, E = p.E;
-  const int t0 = blockIdx.y * kGmTile, e0 = blockIdx.x * kGmTile;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int t0 = blockIdx.y * TT, e0 = blockIdx.x * TE;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   {
     const size_t nmask = (size_t)E * ((T + 31) / 32);
     const size_t gtid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t gsz = (size_t)gridDim.x * gridDim.y * blockDim.x;
     for (size_t i = gtid; i < nmask; i += gsz) p.ws.mask[i] = 0u;
   }
-  // Each 16-wide K step is summed in fp32 and added into a double-float
-  // accumulator (hi, lo).
-  float ah[4][4], al[4][4];
+  float4 wreg[NW];
+  uint4 xreg = make_uint4(0, 0, 0, 0);
+  // Global loads of K step kk: W rows (float4 = 4 consecutive k of one
+  // expert) and token rows (8 bf16 or 4 fp32 consecutive k of one token).
+  auto gload = [&](int kk) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const int idx = tid + i * 256, row = idx >> 2, q = idx & 3, e = e0 + row;
+      wreg[i] = e < E ? *reinterpret_cast<const float4*>(p.wr + (size_t)e * H + kk + q * 4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (XBF16) {
+      if (tid < 2 * TT) {
+        const int row = tid >> 1, hf = tid & 1, t = t0 + row;
+        xreg = t < T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * H + kk + hf * 8)
+                     : make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      const int row = tid >> 2, q = tid & 3, t = t0 + row;
+      xreg = t < T ? *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(p.x) + (size_t)t * H + kk + q * 4)
+                   : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // Store the loaded step k-major into buffer `buf`.
+  auto sstore = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const int idx = tid + i * 256, row = idx >> 2, q = idx & 3;
+      ws_[buf][q * 4 + 0][row] = wreg[i].x;
+      ws_[buf][q * 4 + 1][row] = wreg[i].y;
+      ws_[buf][q * 4 + 2][row] = wreg[i].z;
+      ws_[buf][q * 4 + 3][row] = wreg[i].w;
+    }
+    const uint32_t w[4] = {xreg.x, xreg.y, xreg.z, xreg.w};
+    if (XBF16) {
+      if (tid < 2 * TT) {
+        const int row = tid >> 1, hf = tid & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xs[buf][hf * 8 + 2 * j][row] = __uint_as_float(w[j] << 16);
+          xs[buf][hf * 8 + 2 * j + 1][row] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      }
+    } else {
+      const int row = tid >> 2, q = tid & 3;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xs[buf][q * 4 + j][row] = __uint_as_float(w[j]);
+    }
+  };
+  float ah[4][NE], al[4][NE];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) { ah[i][j] = 0.f; al[i][j] = 0.f; }
-  for (int kk = 0; kk < H; kk += kGmK) {
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      const int idx = threadIdx.x + l * 256;
-      const int r = idx >> 4, c = idx & 15;
-      const int t = t0 + r, e = e0 + r;
-      float xv = 0.f, wv = 0.f;
-      if (t < T)
-        xv = XBF16 ? bf16_f32(reinterpret_cast<const uint16_t*>(p.x)[(size_t)t * H + kk + c])
-                   : reinterpret_cast<const float*>(p.x)[(size_t)t * H + kk + c];
-      if (e < E) wv = p.wr[(size_t)e * H + kk + c];
-      xs[c][r] = xv;
-      ws_[c][r] = wv;
-    }
-    __syncthreads();
-    float acc[4][4];
+    for (int j = 0; j < NE; ++j) { ah[i][j] = 0.f; al[i][j] = 0.f; }
+  gload(0);
+  sstore(0);
+  __syncthreads();
+  int buf = 0;
+  for (int kk = 0; kk < H; kk += KS, buf ^= 1) {
+    const bool more = kk + KS < H;
+    if (more) gload(kk + KS);
+    float acc[4][NE];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < NE; ++j) acc[i][j] = 0.f;
 #pragma unroll
-    for (int c = 0; c < kGmK; ++c) {
-      float a[4], b[4];
+    for (int k = 0; k < KS; ++k) {
+      const float4 a4 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 4]);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+      float b[NE];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[c][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws_[c][tx * 4 + j];
+      for (int j = 0; j < NE; j += 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(&ws_[buf][k][tx * NE + j]);
+        b[j] = b4.x; b[j + 1] = b4.y; b[j + 2] = b4.z; b[j + 3] = b4.w;
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < NE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) df_add_f(ah[i][j], al[i][j], acc[i][j]);
+      for (int j = 0; j < NE; ++j) df_add_f(ah[i][j], al[i][j], acc[i][j]);
+    if (more) sstore(buf ^ 1);
     __syncthreads();
   }
 #pragma unroll
@@ -293,8 +341,8 @@ __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
     const int t = t0 + ty * 4 + i;
     if (t >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
+    for (int j = 0; j < NE; ++j) {
+      const int e = e0 + tx * NE + j;
       if (e < E) {
         float sh, sl;
         df_add(ah[i][j], al[i][j], p.br ? p.br[e] : 0.f, 0.f, sh, sl);
@@ -429,7 +477,9 @@ __global__ void __launch_bounds__(1024) k_plan_from_offsets(BucketParams p, cons
 }
 
 cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s) {
-  const dim3 g1((p.E + kGmTile - 1) / kGmTile, (p.T + kGmTile - 1) / kGmTile);
+  // 64-expert x 64-token tiles: 80 registers, three CTAs per SM (a 128-expert
+  // tile needs 137 registers and one CTA per SM, and was slower).
+  const dim3 g1((p.E + kGmTE - 1) / kGmTE, (p.T + kGmTT - 1) / kGmTT);
   prof_before(MOE_STAGE_ROUTE, s);
   if (p.x_bf16)
     k_router_gemm<true><<<g1, 256, 0, s>>>(p);
