@@ -199,6 +199,17 @@ int moe_forward_static_scratch(const moe_shape* shape, const void* x, int x_dtyp
                                float* out, int accumulate, int32_t* ids_out, float* w_out, int path,
                                int32_t* status_dev, void* stream);
 
+/* Diagnostic of the device-side failure detection: launches one thread that
+ * waits, with the same bounded-wait code the kernels use but a limit of
+ * max_cycles SM clock cycles (1 <= max_cycles <= 4e9), on a barrier that
+ * never completes, then synchronises `stream` and stores the outcome in
+ * *status_out: MOE_ERR_TIMEOUT when the wait gave up as designed.  The GPU
+ * context stays usable.  It borrows 4 bytes of the static scratch region of
+ * moe_forward_static_scratch (do not overlap the two).  No counterpart on the
+ * pages; their runtime gives each test child a deadline [Deltafin's custom
+ * compiled runtime, "One native build and test graph"]. */
+int moe_wait_selftest(long long max_cycles, void* stream, int* status_out);
+
 /* Synchronises `stream`, then reads the device status word of `ws` into
  * *status_out (MOE_OK if no kernel flagged a problem since the last call that
  * began with this workspace).  Returns MOE_ERR_CUDA if the synchronisation or

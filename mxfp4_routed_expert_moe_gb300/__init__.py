@@ -34,7 +34,8 @@ DECODE_MAX_T = 64
 
 # Every symbol the header declares (checked by the tests against the .so).
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_route", "moe_mxfp4_experts",
-           "moe_forward", "moe_device_status", "moe_profile_events", "moe_forward_static_scratch")
+           "moe_forward", "moe_device_status", "moe_profile_events", "moe_forward_static_scratch",
+           "moe_wait_selftest")
 STATIC_SCRATCH_BYTES = 8 << 20
 
 STAGE_ROUTE, STAGE_GATEUP, STAGE_DOWN, STAGE_COMBINE, STAGE_PF_GATEUP, STAGE_PF_DOWN = 1, 2, 3, 4, 5, 6
@@ -80,6 +81,7 @@ def lib():
             L.moe_forward.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp, i32, vp, sz, vp]
             L.moe_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
             L.moe_profile_events.argtypes = [i32, vp, vp]
+            L.moe_wait_selftest.argtypes = [ctypes.c_longlong, vp, P(ctypes.c_int)]
             L.moe_forward_static_scratch.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp,
                                                      i32, vp, vp]
             _LIB = L
@@ -178,6 +180,15 @@ def forward_static_scratch(shp: Shape, x, w_router, b_router, experts, shared, o
                                           _ptr(experts), sh, _ptr(out), int(bool(accumulate)), _ptr(ids_out),
                                           _ptr(w_out), int(path), _ptr(status_dev), _stream(stream))
     _check(rc, "moe_forward_static_scratch")
+
+
+def wait_selftest(max_cycles: int, stream=None) -> int:
+    """moe_wait_selftest: run the device bounded-wait code on a barrier that
+    never completes, with a limit of max_cycles; returns the device status
+    (MOE_ERR_TIMEOUT when the wait gave up)."""
+    st = ctypes.c_int(-1)
+    _check(lib().moe_wait_selftest(int(max_cycles), _stream(stream), ctypes.byref(st)), "moe_wait_selftest")
+    return st.value
 
 
 def profile_events(stage: int, before=None, after=None) -> None:

@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include "async.cuh"
 #include "kernels.h"
 
 using namespace moe;
@@ -158,6 +159,18 @@ int static_scratch_ptr(void** out) {
   return MOE_OK;
 }
 
+// Diagnostic of the bounded-wait mechanism: one thread waits, with the
+// library's wait helper and a limit of max_cycles, on a barrier phase that
+// never completes (two arrivals expected, one made), and records the outcome.
+__global__ void k_wait_selftest(long long max_cycles, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 2);
+  mbar_init_fence();
+  mbar_arrive(&bar);
+  *status = mbar_wait_for(&bar, 0, max_cycles) ? MOE_OK : MOE_ERR_TIMEOUT;
+}
+
 }  // namespace
 
 extern "C" {
@@ -275,6 +288,25 @@ int moe_forward_static_scratch(const moe_shape* shape, const void* x, int x_dtyp
       cudaMemcpyAsync(status_dev, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, (cudaStream_t)stream) !=
           cudaSuccess)
     return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_wait_selftest(long long max_cycles, void* stream, int* status_out) {
+  if (!status_out || max_cycles < 1 || max_cycles > kWaitCycles) return MOE_ERR_INVALID_ARG;
+  // The device status is written into the caller-visible result below; a
+  // 4-byte device word is borrowed from the static scratch region.
+  void* scratch = nullptr;
+  int st = static_scratch_ptr(&scratch);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* dev_status = reinterpret_cast<int*>(scratch);
+  k_wait_selftest<<<1, 32, 0, s>>>(max_cycles, dev_status);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = -1;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *status_out = v;
   return MOE_OK;
 }
 

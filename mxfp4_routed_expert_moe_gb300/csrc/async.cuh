@@ -57,14 +57,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return done != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete, for at most
+// max_cycles SM clock cycles; false on timeout.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, long long max_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > max_cycles) return false;
   }
+}
+
+// Wait for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitCycles);
 }
 
 // Contiguous global -> shared copy by the bulk-copy engine, completing
