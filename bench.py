@@ -169,6 +169,8 @@ class Layer:
         self.ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device=device)
         self.w = torch.empty((wl.T, wl.k), dtype=torch.float32, device=device)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_sink = torch.empty((), dtype=torch.float32, device=device)
         torch.cuda.synchronize()
 
     def step(self):
@@ -176,7 +178,12 @@ class Layer:
                          self.ws, ids_out=self.ids, w_out=self.w)
 
     def flush_l2(self):
+        # Write a buffer larger than L2, then read another one: the step
+        # starts with an L2 holding only clean lines of unrelated data (the
+        # write-backs of the written buffer happen here, not in the step).
         self.flush_buf.fill_(1.0)
+        torch_ = self.torch
+        torch_.amax(self.flush_read, dim=0, out=self.flush_sink)
 
     @property
     def decode_path(self) -> bool:
@@ -542,7 +549,7 @@ def main():
         "data": "synthetic (seeded; 896 experts resident in HBM)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "path": "decode" if layer.decode_path else "prefill", "cuda_graph": not args.no_graph,
-                   "l2": "flushed before every step (256 MiB write, outside the step timing)",
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read; outside the step timing)",
                    "active_experts": n_active, "parallelism": f"replicas x{world}"},
         "weight_gbps": step_bytes / (ms / 1000.0) / 1e9,
         "step_roofline": {"bytes": step_bytes, "frac_hbm": step_bytes / (ms / 1000.0) / 1e9 / hbm,

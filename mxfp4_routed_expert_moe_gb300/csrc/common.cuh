@@ -171,6 +171,44 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[V]) {
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
+// One token row of bf16 activations -> f16 scaled by 2^sigma_t, with sigma_t
+// putting the row's largest magnitude in [2^14, 2^15) (exact: bf16 has 8
+// significant bits); xscale_t = 2^-sigma_t.  Called by all threads of a CTA
+// (any multiple of 32 up to 1024); H % 8 == 0.
+__device__ __forceinline__ void x_row_to_f16(const uint16_t* xb, int H, uint16_t* xo, float* xscale) {
+  __shared__ float xr_wmax[32];
+  float m = 0.f;
+  for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xb + h);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) xr_wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, xr_wmax[w]);
+  int sig = 0;
+  if (m > 0.f) sig = 14 - ((int)((__float_as_uint(m) >> 23) & 0xFF) - 127);
+  sig = sig > 100 ? 100 : (sig < -100 ? -100 : sig);
+  const float up = __int_as_float((sig + 127) << 23);
+  if (threadIdx.x == 0) *xscale = __int_as_float((127 - sig) << 23);
+  for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xb + h);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * up, __uint_as_float(w[j] & 0xFFFF0000u) * up);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(xo + h) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ------------------------------------------------ double-float arithmetic --
 // A value is carried as an unevaluated sum hi + lo of two floats (Knuth's
 // TwoSum / Dekker's Fast2Sum error-free transformations), which keeps router

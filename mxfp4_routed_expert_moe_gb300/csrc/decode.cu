@@ -784,6 +784,357 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
   }
 }
 
+// ------------------------------------ gate/up + SwiGLU on warp tensor cores --
+// bf16 activations, H % 128 == 0.  Item = (active expert u, 8 rows of gate and
+// the same 8 rows of up), stacked as the 16 rows of one m16n8k16 A tile; the
+// MMA's 8 columns are 8 routed pairs of the expert (one pass).  Consumer warp
+// w owns the K-blocks [w*QB, (w+1)*QB), QB = 4*QW, for every item, and keeps
+// the activations of its pass columns for those blocks in registers.
+//   * Thread (g = lane/4, t = lane%4) reads bytes [4t, 4t+4) of each block
+//     (elements 8t..8t+7) of rows g and g+8; one E2M1 byte converts to an
+//     exact f16 pair.  The MMA's logical k is permuted so that its slots
+//     2t, 2t+1, 2t+8, 2t+9 take elements 8t..8t+3 (first MMA) and 8t+4..8t+7
+//     (second); the activation fragment is the same 16 bytes of the pass
+//     column's row, so both operands use one permutation and the dot
+//     product is unchanged.
+//   * Products of an E2M1 value and an f16 activation are exact in the MMA's
+//     fp32 accumulation; the block's sum is multiplied once by 2^(s-127).
+//   * Rows sit at a stride of H/2 + 16 bytes in shared memory (one bulk copy
+//     per row), so the 32 lanes' 4-byte reads fall in 32 distinct banks.
+// Warps' partial sums are added by the reducer warp in warp order, and each
+// column's arithmetic is independent of the other columns: a pair's result
+// does not depend on the rest of the batch.
+constexpr int kGmRows = 16;    // rows per item (8 gate over 8 up)
+constexpr int kGmCols = 8;     // routed pairs per pass
+constexpr int kGmMaxWarps = 14;   // consumer warps
+constexpr int kGmProducers = 1;   // producer warps (alternate stages)
+
+struct GmRedMeta {
+  int r0;
+  int b0;
+  int n;
+  int pass;
+  int release;  // stage to hand back to the producers after this pass, or -1
+};
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+  return v;
+}
+
+// Bit 7 of a byte of the result is set when that byte of w is 0 or 255 (the
+// E8M0 codes that are not a plain exponent field: 2^-127 is subnormal, 255 is
+// NaN); other bits are don't-care.
+__device__ __forceinline__ uint32_t e8m0_special4(uint32_t w) {
+  return ((w - 0x01010101u) & ~w) | ((0xFEFEFEFEu - w) & w);
+}
+
+
+// One K-block of the 16-row tile: acc += (A_blk . B_blk) * 2^(s-127) per row.
+template <bool PLAIN, int J>
+__device__ __forceinline__ void gm_block(const uint8_t* ag, const uint8_t* au, const uint4 xb, uint32_t sg,
+                                         uint32_t su, float (&acc)[4]) {
+  const uint32_t wg = lds32(ag), wu = lds32(au);
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[4];
+  mma_f16_16816(d, e2m1x2_f16x2(wg, 0), e2m1x2_f16x2(wu, 0), e2m1x2_f16x2(wg, 1), e2m1x2_f16x2(wu, 1), xb.x, xb.y,
+                zero);
+  mma_f16_16816(d, e2m1x2_f16x2(wg, 2), e2m1x2_f16x2(wu, 2), e2m1x2_f16x2(wg, 3), e2m1x2_f16x2(wu, 3), xb.z, xb.w,
+                d);
+  float fg, fu;
+  if (PLAIN) {
+    fg = __uint_as_float(((sg >> (8 * J)) & 0xFFu) << 23);
+    fu = __uint_as_float(((su >> (8 * J)) & 0xFFu) << 23);
+  } else {
+    fg = e8m0_f32((sg >> (8 * J)) & 0xFFu);
+    fu = e8m0_f32((su >> (8 * J)) & 0xFFu);
+  }
+  acc[0] = fmaf(d[0], fg, acc[0]);
+  acc[1] = fmaf(d[1], fg, acc[1]);
+  acc[2] = fmaf(d[2], fu, acc[2]);
+  acc[3] = fmaf(d[3], fu, acc[3]);
+}
+
+// One pass over the warp's QW quads of K-blocks with the scales taken as plain
+// exponent fields; the scales of rows g and g+8 are read as one word per 4
+// blocks from sgp / sup.  Returns nonzero when one of them was 0 or 255 (the
+// pass must then be redone by gm_pass_exact).
+template <int QW>
+__device__ __forceinline__ uint32_t gm_pass(const uint8_t* ag, const uint8_t* au, const uint4 (&xb)[4 * QW],
+                                            const uint8_t* sgp, const uint8_t* sup, float (&acc)[4]) {
+  uint32_t spec = 0u;
+#pragma unroll
+  for (int q = 0; q < QW; ++q) {
+    const uint32_t sg = lds32(sgp + 4 * q), su = lds32(sup + 4 * q);
+    spec |= e8m0_special4(sg) | e8m0_special4(su);
+    gm_block<true, 0>(ag + 64 * q, au + 64 * q, xb[4 * q], sg, su, acc);
+    gm_block<true, 1>(ag + 64 * q + 16, au + 64 * q + 16, xb[4 * q + 1], sg, su, acc);
+    gm_block<true, 2>(ag + 64 * q + 32, au + 64 * q + 32, xb[4 * q + 2], sg, su, acc);
+    gm_block<true, 3>(ag + 64 * q + 48, au + 64 * q + 48, xb[4 * q + 3], sg, su, acc);
+  }
+  return spec & 0x80808080u;
+}
+
+// The same pass with every scale converted exactly, block by block (kept
+// compact: it runs only for weights holding the codes 0 or 255); the
+// activation fragments are read again from xr (null: zeros).
+__device__ __noinline__ void gm_pass_exact(const uint8_t* ag, const uint8_t* au, const uint16_t* xr,
+                                           const uint8_t* sgp, const uint8_t* sup, int nblk, float (&acc)[4]) {
+#pragma unroll 1
+  for (int j = 0; j < nblk; ++j) {
+    const uint4 x = xr ? *reinterpret_cast<const uint4*>(xr + j * 32) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t sg = sgp[j], su = sup[j];
+    gm_block<false, 0>(ag + 16 * j, au + 16 * j, x, sg, su, acc);
+  }
+}
+
+__host__ __device__ inline uint32_t gm_row_stride(int H) { return (uint32_t)(H / 2 + 16); }
+__host__ __device__ inline uint32_t gm_stage_bytes(int H) {
+  const uint32_t b = (uint32_t)kGmRows * gm_row_stride(H) + (uint32_t)kGmRows * (uint32_t)(H / 32);
+  return (b + 127u) & ~127u;
+}
+
+template <int QW>
+__global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
+    k_dec_gateup_mma(ExpertParams p, int stages, uint32_t stage_bytes) {
+  constexpr int QB = 4 * QW;  // K-blocks per consumer warp
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ Ring rs;
+  __shared__ float2 red[2][kGmMaxWarps][kGmRows][kGmCols / 2];
+  __shared__ GmRedMeta rmeta[2];
+  __shared__ float xs_s[kDecodeMaxT];
+  const int H = p.H, I = p.I, k = p.k;
+  const int nbH = H / 32;
+  const int W = nbH / QB;  // consumer warps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t qrow = (uint32_t)(H / 2), qs = gm_row_stride(H);
+  const uint32_t sc_off = (uint32_t)kGmRows * qs;
+  uint8_t* ring_data = smem;
+  const size_t ring_bytes = (size_t)stages * stage_bytes;
+  const size_t scratch_bytes = p.fused_route ? route_small_scratch_bytes(p.E, blockDim.x / 32, p.T) : 0;
+  Plan pl = plan_carve(p, smem + (ring_bytes > scratch_bytes ? ring_bytes : scratch_bytes), 4);
+  if (threadIdx.x == 0) {
+    // The reducer hands a stage back once it has read the partial sums of
+    // the item's last pass (every consumer warp has finished reading the
+    // stage by then).
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&rs.full[s], 1);
+      mbar_init(&rs.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&rs.red_full[s], W);
+      mbar_init(&rs.red_empty[s], 1);
+    }
+    rs.abort_flag = 0;
+    mbar_init_fence();
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < (H + 31) / 32; i += blockDim.x) p.ws.rowdone[i] = 0u;
+  for (int t = threadIdx.x; t < p.T; t += blockDim.x) xs_s[t] = p.ws.xscale[t];
+  if (p.fused_route) {
+    SmallPlan sp;
+    sp.ue = pl.ue;
+    sp.ub0 = pl.ub0;
+    sp.un = pl.un;
+    sp.pairs = pl.pairs;
+    route_small(p.rp, reinterpret_cast<char*>(ring_data), sp, blockIdx.x == 0);
+    pl.U = sp.U;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else {
+    load_plan(p, pl);
+  }
+  __syncthreads();
+  plan_cache_ptrs(p, pl, 0);
+  __syncthreads();
+  const int tiles = I / 8;
+  const int n_items = pl.U * tiles;
+  // Every item costs the same weight bytes: each CTA takes a contiguous range
+  // (consecutive items share an expert, so the consumers' activation
+  // registers stay valid), and two producer warps fill alternate stages.
+  const int beg = (int)((long long)n_items * blockIdx.x / gridDim.x);
+  const int n_mine = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x) - beg;
+
+  if (warp >= W && warp < W + kGmProducers) {  // producers: 18 lanes issue one item's copies
+    int issued_use[kMaxStages];
+    for (int i = 0; i < kMaxStages; ++i) issued_use[i] = -1;
+    bool ok = true;
+    for (int it = warp - W;; it += kGmProducers) {
+      const int s = it % stages, use = it / stages;
+      const int item = it < n_mine ? beg + it : -1;
+      if (lane == 0) {
+        if (use > 0 && !mbar_wait(&rs.empty[s], (use - 1) & 1)) ok = false;
+        if (ok && *(volatile int*)&rs.abort_flag) ok = false;
+        if (ok) rs.item[s] = item;
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      uint64_t* bar = &rs.full[s];
+      if (item < 0) {
+        if (lane == 0) mbar_arrive(bar);
+        break;
+      }
+      const int u = item / tiles, rt = item % tiles;
+      const uint8_t* const* pp = pl.ptrs + u * 4;
+      if (!pp[0]) {  // bad descriptor: flagged in the plan, not read
+        if (lane == 0) mbar_arrive(bar);
+        continue;
+      }
+      const size_t r0 = (size_t)rt * 8;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)kGmRows * qrow + (uint32_t)kGmRows * (uint32_t)nbH);
+        issued_use[s] = use;
+      }
+      __syncwarp();
+      uint8_t* st = ring_data + (size_t)s * stage_bytes;
+      if (lane < kGmRows)
+        bulk_g2s(st + (size_t)lane * qs, pp[lane >> 3] + (r0 + (lane & 7)) * qrow, qrow, bar);
+      else if (lane < kGmRows + 2)
+        bulk_g2s(st + sc_off + (size_t)(lane - kGmRows) * 8 * nbH, pp[2 + lane - kGmRows] + r0 * nbH,
+                 (uint32_t)(8 * nbH), bar);
+    }
+    if (!ok && lane == 0) {
+      set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+      rs.abort_flag = 1;
+      for (int s = 0; s < stages; ++s)
+        if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
+    }
+    return;
+  }
+
+  float* hout = reinterpret_cast<float*>(p.ws.h);
+  if (warp == W + kGmProducers) {  // reducer: lane = (row r = lane/4, columns 2(lane%4), +1)
+    const int r = lane >> 2, c = 2 * (lane & 3);
+    for (int pc = 0;; ++pc) {
+      const int slot = pc & 1;
+      if (!mbar_wait(&rs.red_full[slot], (pc >> 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        break;
+      }
+      const GmRedMeta m = rmeta[slot];
+      if (m.r0 < 0) break;
+      if (lane == 0 && m.release >= 0) mbar_arrive(&rs.empty[m.release]);  // all warps are past the stage
+      float2 gs = make_float2(0.f, 0.f), us = make_float2(0.f, 0.f);
+      for (int w = 0; w < W; ++w) {
+        const float2 a = red[slot][w][r][c >> 1], b = red[slot][w][r + 8][c >> 1];
+        gs.x += a.x;
+        gs.y += a.y;
+        us.x += b.x;
+        us.y += b.y;
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int col = m.pass + c + i;
+        if (col < m.n) {
+          const int ent = pl.pairs[m.b0 + col];
+          if (ent >= 0) {
+            const float xs = xs_s[ent / k];
+            const float g = (i ? gs.y : gs.x) * xs, uu = (i ? us.y : us.x) * xs;
+            hout[(size_t)ent * I + h_swz(m.r0 + r)] = silu_f32(g) * uu;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_empty[slot]);
+    }
+    return;
+  }
+
+  // consumers
+  const int g = lane >> 2, t = lane & 3;
+  const int kb0 = warp * QB;  // first K-block of this warp
+  uint4 xb[QB];
+#pragma unroll
+  for (int j = 0; j < QB; ++j) xb[j] = make_uint4(0u, 0u, 0u, 0u);
+  int xt = -1;  // token whose activations are in xb (-1: zeros)
+  int pc = 0;
+  bool dead = false;
+  for (int it = 0;; ++it) {
+    const int s = it % stages, use = it / stages;
+    if (!mbar_wait(&rs.full[s], use & 1)) {
+      set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+      rs.abort_flag = 1;
+      break;
+    }
+    const int item = rs.item[s];
+    if (item < 0) break;
+    const int u = item / tiles, rt = item % tiles;
+    const int b0 = pl.ub0[u], n = pl.un[u];
+    const uint8_t* st = ring_data + (size_t)s * stage_bytes;
+    const uint8_t* ag = st + (size_t)g * qs + (size_t)kb0 * 16 + 4 * t;
+    const uint8_t* au = ag + (size_t)8 * qs;
+    const uint8_t* sgp = st + sc_off + (size_t)g * nbH + kb0;
+    const uint8_t* sup = sgp + (size_t)8 * nbH;
+    const int npass = n > 0 ? (n + kGmCols - 1) / kGmCols : 1;  // a pass also hands the stage back
+    for (int pi = 0; pi < npass; ++pi) {
+      const int pass = pi * kGmCols;
+      const int pe = pass + g < n ? pl.pairs[b0 + pass + g] : -1;
+      const int tok = pe >= 0 ? pe / k : -1;
+      if (tok != xt) {
+        if (tok >= 0) {
+          const uint16_t* xr = p.ws.xh + (size_t)tok * H + (size_t)kb0 * 32 + 8 * t;
+#pragma unroll
+          for (int j = 0; j < QB; ++j) xb[j] = *reinterpret_cast<const uint4*>(xr + j * 32);
+        } else {
+#pragma unroll
+          for (int j = 0; j < QB; ++j) xb[j] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        xt = tok;
+      }
+      __syncwarp();
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // Scale codes 0 and 255 need the exact conversion: the pass is redone
+      // (warp-uniform: the MMAs need all lanes).
+      if (__any_sync(0xFFFFFFFFu, gm_pass<QW>(ag, au, xb, sgp, sup, acc) != 0u)) {
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        gm_pass_exact(ag, au, tok >= 0 ? p.ws.xh + (size_t)tok * H + (size_t)kb0 * 32 + 8 * t : nullptr, sgp, sup,
+                      QB, acc);
+      }
+      const int slot = pc & 1;
+      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        dead = true;
+        break;
+      }
+      red[slot][warp][g][t] = make_float2(acc[0], acc[1]);
+      red[slot][warp][g + 8][t] = make_float2(acc[2], acc[3]);
+      if (warp == 0 && lane == 0) {
+        GmRedMeta m;
+        m.r0 = rt * 8;
+        m.b0 = b0;
+        m.n = n;
+        m.pass = pass;
+        m.release = pi == npass - 1 ? s : -1;
+        rmeta[slot] = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+      ++pc;
+    }
+    if (dead) break;
+  }
+  // Tell the reducer there is no more work.
+  {
+    const int slot = pc & 1;
+    if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
+    if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+  }
+}
+
 // -------------------------------------------------------- down + combine --
 // Item = (active expert u, tile of 64 rows of Wd), one contiguous bulk copy.
 // Warp w owns block columns 4w..4w+3 of all 64 rows; lane l owns block column
@@ -1044,12 +1395,63 @@ static bool tma_path_ok(const ExpertParams& p) {
 }
 
 template <int NT>
+static cudaError_t launch_decode_down(const ExpertParams& p, cudaStream_t s, size_t smem_max);
+
+// K-blocks per consumer warp of the tensor-core gate/up kernel, in quads of
+// 4 blocks (0: the kernel does not apply to this shape / dtype).
+static int gm_quads_per_warp(const ExpertParams& p) {
+  if (!p.x_bf16 || p.H % 128 != 0 || p.I % 8 != 0) return 0;
+  const int quads = p.H / 128;
+  for (int qw = 1; qw <= 4; qw *= 2)
+    if (quads % qw == 0 && quads / qw <= kGmMaxWarps) return qw;
+  return 0;
+}
+
+template <int QW>
+static cudaError_t launch_gateup_mma(const ExpertParams& p, cudaStream_t s, size_t smem_max) {
+  const int W = p.H / 128 / QW;
+  const int threads = (W + kGmProducers + 1) * 32;
+  auto kern = k_dec_gateup_mma<QW>;
+  // The dynamic ring and plan share the SM's 227 KB with the static arrays.
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, (const void*)kern);
+  if (err != cudaSuccess) return err;
+  const size_t cap = (size_t)227 * 1024 - fa.sharedSizeBytes;
+  smem_max = smem_max < cap ? smem_max : cap;
+  const size_t plan = plan_smem_bytes(p.E, p.T * p.k, 4);
+  const uint32_t stage = gm_stage_bytes(p.H);
+  int stages = (int)((smem_max - plan) / stage);
+  stages = stages > kMaxStages ? kMaxStages : stages;
+  if (stages < 2) return cudaErrorNotSupported;
+  size_t front = (size_t)stages * stage;
+  if (p.fused_route) {
+    const size_t scratch = route_small_scratch_bytes(p.E, threads / 32, p.T);
+    if (scratch > front) front = scratch;
+  }
+  const size_t smem = front + plan;
+  if (smem > smem_max) return cudaErrorNotSupported;
+  if (!p.fused_route && (err = launch_x_to_f16(p, s)) != cudaSuccess) return err;
+  if ((err = ensure_smem_attr((const void*)kern, smem)) != cudaSuccess) return err;
+  prof_before(MOE_STAGE_GATEUP, s);
+  err = launch_pdl(kern, dim3(device_sm_count()), dim3(threads), smem, s, p, stages, stage);
+  prof_after(MOE_STAGE_GATEUP, s);
+  return err;
+}
+
+template <int NT>
 static cudaError_t launch_decode_tma(const ExpertParams& p, cudaStream_t s) {
   constexpr int R = kGuRowsNT / NT;
   const int nsm = device_sm_count();
   cudaError_t err;
   const size_t smem_max = 200 * 1024;
   // gate/up (+ routing prologue)
+  const int qw = gm_quads_per_warp(p);
+  if (qw) {
+    err = qw == 1 ? launch_gateup_mma<1>(p, s, smem_max)
+                  : (qw == 2 ? launch_gateup_mma<2>(p, s, smem_max) : launch_gateup_mma<4>(p, s, smem_max));
+    if (err != cudaSuccess) return err;
+    return launch_decode_down<NT>(p, s, smem_max);
+  }
   const int nbH = p.H / 32;
   const int ncw = (nbH + 31) / 32;
   const int gu_threads = kGuGroups * ncw * 32 + 64;
@@ -1071,7 +1473,14 @@ static cudaError_t launch_decode_tma(const ExpertParams& p, cudaStream_t s) {
   err = launch_pdl(gu, dim3(nsm), dim3(gu_threads), gu_smem, s, p, gu_stages, gu_stage);
   prof_after(MOE_STAGE_GATEUP, s);
   if (err != cudaSuccess) return err;
-  // down (+ combine)
+  return launch_decode_down<NT>(p, s, smem_max);
+}
+
+// down (+ combine)
+template <int NT>
+static cudaError_t launch_decode_down(const ExpertParams& p, cudaStream_t s, size_t smem_max) {
+  cudaError_t err;
+  const int nsm = device_sm_count();
   const int nbI = p.I / 32;
   const size_t dn_plan = plan_smem_bytes(p.E, p.T * p.k, 2);
   const uint32_t dn_stage = (uint32_t)(kDnRows * (p.I / 2) + kDnRows * nbI + NT * p.I * 4);

@@ -66,5 +66,7 @@ constexpr int kPfMTile = 128;   // weight rows per MMA tile (M)
 // slices; 4-byte scale rows) and bf16 activations.
 bool prefill_supported(int H, int I);
 cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s);
+// bf16 activations -> ws.xh (f16, per-token power-of-two shift) and ws.xscale.
+cudaError_t launch_x_to_f16(const ExpertParams& p, cudaStream_t s);
 
 }  // namespace moe

@@ -71,44 +71,16 @@ struct PfRaw {
 static_assert(kPfEpWarps == 4 && (kPfDqWarps + kPfLdWarps) % 4 == 0, "epilogue warps must cover lane quarters 0-3");
 
 // ------------------------------------------------------------ pre-passes --
-// xh[t][h] = f16(x[t][h] * 2^sigma_t), xscale[t] = 2^-sigma_t, with sigma_t
-// putting the token's largest magnitude in [2^14, 2^15).
+// xh[t][h] = f16(x[t][h] * 2^sigma_t), xscale[t] = 2^-sigma_t (one CTA per token).
 __global__ void __launch_bounds__(256) k_x_to_f16(ExpertParams p) {
-  __shared__ float wmax[8];
   const int t = blockIdx.x;
-  const int H = p.H;
-  const uint16_t* xb = reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * H;
-  float m = 0.f;
-  for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xb + h);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
-  __syncthreads();
-  m = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
-  int sig = 0;
-  if (m > 0.f) sig = 14 - ((int)((__float_as_uint(m) >> 23) & 0xFF) - 127);
-  sig = sig > 100 ? 100 : (sig < -100 ? -100 : sig);
-  const float up = __int_as_float((sig + 127) << 23);
-  if (threadIdx.x == 0) p.ws.xscale[t] = __int_as_float((127 - sig) << 23);
-  uint16_t* xo = p.ws.xh + (size_t)t * H;
-  for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xb + h);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * up, __uint_as_float(w[j] & 0xFFFF0000u) * up);
-      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint4*>(xo + h) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+  x_row_to_f16(reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * p.H, p.H, p.ws.xh + (size_t)t * p.H,
+               &p.ws.xscale[t]);
+}
+
+cudaError_t launch_x_to_f16(const ExpertParams& p, cudaStream_t s) {
+  k_x_to_f16<<<p.T, 256, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 // Row shifts of the bf16 shared expert: shsig[r] = 14 - floor(log2 max|row|)

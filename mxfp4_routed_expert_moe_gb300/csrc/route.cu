@@ -115,6 +115,15 @@ __global__ void __launch_bounds__(kRgThreads) k_router_gemv(RouteParams p) {
     bulk_g2s(rsm, p.wr + (size_t)e0 * H, (uint32_t)(nrows * H * 4), &bar);
   }
   pdl_trigger();
+  // The decode expert kernels read the activations as f16 with a per-token
+  // shift: CTA b converts tokens b, b + gridDim.x, .. (bf16 input) while its
+  // copy lands.
+  if (XBF16)
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      x_row_to_f16(reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * H, H, p.ws.xh + (size_t)t * H,
+                   &p.ws.xscale[t]);
+      __syncthreads();  // x_row_to_f16 reuses its shared maxima
+    }
   __syncthreads();
   bool rows_ready = false;
   for (int tp = 0; tp < T; tp += 2) {

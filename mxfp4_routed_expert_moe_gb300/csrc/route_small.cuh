@@ -96,8 +96,9 @@ __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v)
 }
 
 // Top-k by one warp over packed keys in shared memory (destroyed): lane j < k
-// returns slot j's expert.
-__device__ __forceinline__ int warp_topk_keys(unsigned long long* keys, int E, int k) {
+// returns slot j's expert.  k rounds of warp argmax; after each round only
+// the winning lane rescans its entries.
+__device__ __forceinline__ int warp_topk_keys_rounds(unsigned long long* keys, int E, int k) {
   const int lane = threadIdx.x & 31;
   int my_e = -1;
   unsigned long long lb = lane_best_key(keys, E, lane);
@@ -112,6 +113,65 @@ __device__ __forceinline__ int warp_topk_keys(unsigned long long* keys, int E, i
     __syncwarp();
   }
   return my_e;
+}
+
+// Ascending bitonic sort of 64 keys held as element lane (x0) and element
+// lane + 32 (x1).  Element i pairs with i ^ j; it keeps the smaller key when
+// it is the lower of the two and its block of size k sorts upward.
+__device__ __forceinline__ void warp_sort64(unsigned long long& x0, unsigned long long& x1) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j >= 1; j >>= 1) {
+      if (j == 32) {
+        const unsigned long long lo = x0 < x1 ? x0 : x1, hi = x0 < x1 ? x1 : x0;
+        x0 = lo;
+        x1 = hi;
+      } else {
+        const unsigned long long p0 = __shfl_xor_sync(0xFFFFFFFFu, x0, j);
+        const unsigned long long p1 = __shfl_xor_sync(0xFFFFFFFFu, x1, j);
+        const bool lower = (lane & j) == 0;
+        const bool min0 = lower == ((lane & k) == 0);
+        const bool min1 = lower == (((lane + 32) & k) == 0);
+        x0 = min0 ? (p0 < x0 ? p0 : x0) : (p0 < x0 ? x0 : p0);
+        x1 = min1 ? (p1 < x1 ? p1 : x1) : (p1 < x1 ? x1 : p1);
+      }
+    }
+  }
+}
+
+// Top-k (k <= 32) by one warp over packed keys in shared memory; lane j < k
+// returns slot j's expert.  Each lane keeps its three largest keys; the two
+// largest of every lane (64 keys) are sorted, giving a candidate k-th key K.
+// A key left out is at most its lane's third largest, so when no lane's third
+// largest exceeds K the sorted candidates hold the whole top k (the usual
+// case).  Otherwise the k-round selection runs (it overwrites `keys`).  Keys
+// are unique (the expert index is part of the key): the result is the same
+// either way.
+__device__ __forceinline__ int warp_topk_keys(unsigned long long* keys, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long b1 = 0ull, b2 = 0ull, b3 = 0ull;
+  for (int e0 = lane; e0 < E; e0 += 32 * 8) {
+    unsigned long long v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = e0 + 32 * q < E ? keys[e0 + 32 * q] : 0ull;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const unsigned long long x = v[q];
+      const bool g1 = x > b1, g2 = x > b2, g3 = x > b3;
+      b3 = g2 ? b2 : (g3 ? x : b3);
+      b2 = g1 ? b1 : (g2 ? x : b2);
+      b1 = g1 ? x : b1;
+    }
+  }
+  unsigned long long x0 = b1, x1 = b2;
+  warp_sort64(x0, x1);
+  // Slot j is the (j+1)-th largest: element 63 - j, i.e. x1 of lane 31 - j.
+  const unsigned long long best = __shfl_sync(0xFFFFFFFFu, x1, 31 - lane);
+  const unsigned long long kth = __shfl_sync(0xFFFFFFFFu, x1, 32 - k);
+  if (__any_sync(0xFFFFFFFFu, b3 > kth)) return warp_topk_keys_rounds(keys, E, k);
+  return lane < k ? 4095 - (int)(best & 0xFFFull) : -1;
 }
 
 // Softmax of the selected scores held by lanes 0..k-1 (slot order): lane j
@@ -163,6 +223,8 @@ static __device__ void route_small(const RouteParams& p, char* scratch, SmallPla
   int* off = cnt + E;                                                           // [E+1]
   int* s_ids = off + E + 1;                                                     // [T*k]
   s_ids = reinterpret_cast<int*>((reinterpret_cast<uintptr_t>(s_ids) + 15) & ~(uintptr_t)15);
+  // One key row per token routed at once (at most min(rwarps, T), as
+  // route_small_scratch_bytes counts them).
   unsigned long long* keyrows = reinterpret_cast<unsigned long long*>(s_ids + kDecodeMaxT * kMaxK);
   __shared__ int s_wtot[32][2];
   __shared__ int s_nact;
@@ -170,12 +232,22 @@ static __device__ void route_small(const RouteParams& p, char* scratch, SmallPla
   __syncthreads();
   for (int t0 = 0; t0 < T; t0 += rwarps) {
     const int nt = T - t0 < rwarps ? T - t0 : rwarps;
-    // Scores -> packed keys for tokens t0 .. t0+nt-1, by all threads.
+    // Scores -> packed keys for tokens t0 .. t0+nt-1, by all threads; eight
+    // loads in flight per thread before their stores.
     const int n = nt * E;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const int tt = i / E, e = i - tt * E;
-      keyrows[i] = packed_key(__ldcg(&p.ws.logits[(size_t)(t0 + tt) * E + e]), e);
+    const float2* lg = p.ws.logits + (size_t)t0 * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+      float2 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * (int)blockDim.x;
+        v[q] = i < n ? __ldcg(&lg[i]) : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * (int)blockDim.x;
+        if (i < n) keyrows[i] = packed_key(v[q], i % E);
+      }
     }
     __syncthreads();
     if (warp < nt) {

@@ -132,6 +132,12 @@ EDGE = [
     ("k32", 2, 128, 40, 32, 32),
     ("t64", 64, 64, 24, 4, 64),
     ("f32_many", 33, 128, 12, 2, 64),
+    # Tensor-core gate/up kernel (bf16 activations, H % 128 == 0): more tokens
+    # than router CTAs, items with several 8-pair passes, 1..4 consumer warps.
+    ("mma_t64_passes", 64, 512, 16, 4, 256),
+    ("mma_t40_all_shared", 40, 256, 8, 8, 128),
+    ("mma_h384_odd_warps", 5, 384, 12, 3, 128),
+    ("mma_h128_one_warp", 9, 128, 6, 2, 64),
 ]
 
 
@@ -239,3 +245,31 @@ def test_misaligned_expert_descriptor_is_flagged_not_read():
     out, ids, w = L.forward(path=1)
     assert L.status() == 0
     check_out(out.cpu().numpy(), oracle_out(inp, np.arange(wl.T)), "after misaligned")
+
+
+def test_special_scale_codes_decode():
+    """E8M0 code 0 (2^-127, subnormal) and 255 (NaN) in the expert scales take
+    the exact scale conversion: finite results match the oracle, and a token
+    routed to an expert with a NaN scale comes out NaN where the oracle's does."""
+    wl = _small_workload("mma_specials", 6, 256, 8, 2, 128)
+    inp = synth.make_inputs(wl, seed=11)
+    for e in range(wl.E):
+        ex = inp.expert(e)
+        ex["gate_s"].reshape(-1)[::7] = 0
+        ex["up_s"].reshape(-1)[3::11] = 0
+    inp.expert(3)["up_s"].reshape(-1)[5] = 255
+    L = DeviceLayer(inp)
+    out, ids, w = L.forward(path=1)
+    torch().cuda.synchronize()
+    assert L.status() == 0
+    _, same = check_route(inp, ids.cpu().numpy(), w.cpu().numpy())
+    toks = np.nonzero(same)[0]
+    ref = oracle_out(inp, toks)
+    got = out.cpu().numpy()[toks].astype(np.float64)
+    nan_ref = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan_ref)
+    fin = ~nan_ref.any(axis=1)
+    assert fin.any()
+    check_out(got[fin], ref[fin], "special scales")
+    routed3 = (ids.cpu().numpy()[toks] == 3).any(axis=1)
+    assert np.array_equal(nan_ref.all(axis=1), routed3)
