@@ -190,11 +190,13 @@ class Layer:
         return self.wl.T <= self.moe.DECODE_MAX_T or self.wl.x_dtype == "f32"
 
     def launches_per_step(self) -> int:
-        # decode: router(+top-k tail), gate/up, down(+combine)
         # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
         # shifts), gate/up, down
         if self.decode_path:
-            return 3  # router (+ fused top-k/bucketing), gate/up, down (+ fused combine)
+            wl = self.wl
+            if wl.x_dtype != "f32" and wl.H % 128 == 0 and wl.I % 128 == 0:
+                return 4  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down, combine
+            return 3  # router, gate/up (+ fused top-k/bucketing), down (+ fused combine)
         return 7 + (1 if self.shared is not None else 0)
 
     def dominant_stage(self):
