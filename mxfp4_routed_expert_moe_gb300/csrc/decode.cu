@@ -1060,6 +1060,18 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
 #pragma unroll
   for (int j = 0; j < QB; ++j) xb[j] = make_uint4(0u, 0u, 0u, 0u);
   int xt = -1;  // token whose activations are in xb (-1: zeros)
+  // The first item's activations are read now, ahead of the burst of weight
+  // copies that all CTAs start at once.
+  if (n_mine > 0) {
+    const int u = beg / tiles, n = pl.un[u];
+    const int pe = g < n ? pl.pairs[pl.ub0[u] + g] : -1;
+    if (pe >= 0) {
+      xt = pe / k;
+      const uint16_t* xr = p.ws.xh + (size_t)xt * H + (size_t)kb0 * 32 + 8 * t;
+#pragma unroll
+      for (int j = 0; j < QB; ++j) xb[j] = *reinterpret_cast<const uint4*>(xr + j * 32);
+    }
+  }
   int pc = 0;
   bool dead = false;
   for (int it = 0;; ++it) {
