@@ -193,10 +193,7 @@ class Layer:
         # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
         # shifts), gate/up, down
         if self.decode_path:
-            wl = self.wl
-            if wl.x_dtype != "f32" and wl.H % 128 == 0 and wl.I % 128 == 0:
-                return 4  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down, combine
-            return 3  # router, gate/up (+ fused top-k/bucketing), down (+ fused combine)
+            return 3  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
         return 7 + (1 if self.shared is not None else 0)
 
     def dominant_stage(self):
