@@ -1,18 +1,20 @@
-// decode.cu — weight-streaming MXFP4 expert GEMV for small batches (T <= 64).
+// decode.cu — weight-streaming MXFP4 expert kernels for small batches (T <= 64).
 //
 // The fused MXFP4 dequant+GEMV of [deltafin, "The techniques that bought the
 // 82x"] (16-entry table lookup, E8M0 scale as a power of two on the fp32
 // exponent) is re-designed for the GPU:
-//   * each thread owns one 32-element block column of the weight matrix and
-//     keeps the matching activations of up to NT tokens in registers, so the
-//     weights stream from HBM exactly once per routed expert (tokens sharing
-//     an expert reuse the same load);
-//   * one 128-bit load is one MX block (32 nibbles); two E2M1 codes convert to
-//     an exact f16x2 with one cvt, then to fp32 for the FMAs; the block's
-//     partial sum is scaled once by 2^(e-127), which is exact;
-//   * partial sums are reduced across the warp by a transpose-reduce and
-//     across warps in a fixed order, so each token's result does not depend
-//     on the batch;
+//   * the weights of each routed expert stream from HBM once (bulk copies into
+//     a shared-memory ring fed by a producer warp); tokens sharing an expert
+//     reuse the same pass;
+//   * two E2M1 codes convert to an exact f16x2 with one cvt; each 32-element
+//     block's partial sum is scaled once by 2^(e-127), which is exact;
+//   * gate/up with bf16 activations (k_dec_gateup_mma) multiplies on warp
+//     tensor cores: m16n8k16 MMAs over 8 gate + 8 up rows against 8 routed
+//     pairs, the activations carried as f16 with a per-token power-of-two
+//     shift so that every product is exact; the other decode kernels sum
+//     exact products on CUDA cores, one MX block column per thread;
+//   * partial sums are added across lanes and warps in a fixed order, so each
+//     token's result does not depend on the batch;
 //   * the k expert outputs of a token are combined in slot order ([Deltafin's
 //     custom compiled runtime, "The native build"]: ordered reduction).
 #include <utility>
