@@ -194,14 +194,15 @@ def test_exact_ties_pick_lower_index():
     check_route(inp, ids, w)
 
 
-def test_bad_expert_id_sets_device_status():
+@pytest.mark.parametrize("H", [64, 256], ids=["cuda_core_gateup", "tensor_core_gateup"])
+def test_bad_expert_id_sets_device_status(H):
     t = torch()
-    wl = _small_workload("badid", 4, 64, 8, 2, 64)
+    wl = _small_workload("badid", 4, H, 8, 2, 128)
     inp = synth.make_inputs(wl, seed=1)
     L = DeviceLayer(inp)
     ids = t.tensor([[0, 1], [2, 99], [3, 4], [5, 6]], dtype=t.int32, device="cuda")
     w = t.full((4, 2), 0.5, dtype=t.float32, device="cuda")
-    out = t.zeros((4, 64), dtype=t.float32, device="cuda")
+    out = t.zeros((4, H), dtype=t.float32, device="cuda")
     L.moe.mxfp4_experts(L.shape, L.x, L.table.desc, ids, w, None, None, out, False, L.ws, path=1)
     assert L.status() == L.moe.MOE_ERR_DEVICE_CHECK
     # The next call on the same workspace starts clean.
