@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload decode|wide|prefill|long|decode_i1536|tiny]
+    python bench.py --sweep [--sweep-i 1408|1536] [--steps K]
 
 A step is one pass of the whole layer (moe_forward: router, top-k, bucketing,
 MXFP4 experts, combine) over one batch of the workload.  The default workload
@@ -45,6 +46,9 @@ def parse_args():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time both paths over batch sizes T (one JSON line per T and path) instead of one workload")
+    ap.add_argument("--sweep-i", type=int, default=1408, choices=[1408, 1536], help="intermediate size of the sweep")
     return ap.parse_args()
 
 
@@ -139,19 +143,26 @@ class ClockSampler:
 class Layer:
     """The workload resident on one GPU, called through the C ABI."""
 
-    def __init__(self, wl_name: str, device: str):
+    def __init__(self, wl, device: str, table=None, path=None):
+        """wl: a workload or its name.  table: an ExpertTable already filled
+        with this workload's experts (they depend on H, E, I and the seed
+        only), else one is made and filled.  path: the library's path
+        selector (default: its own choice by T)."""
         import torch
 
         import mxfp4_routed_expert_moe_gb300 as moe
         import synth
         self.torch, self.moe, self.synth = torch, moe, synth
-        self.wl = wl = synth.WORKLOADS[wl_name]
+        self.wl = wl = synth.WORKLOADS[wl] if isinstance(wl, str) else wl
         self.inp = inp = synth.make_inputs(wl)
         self.device = device
-        self.table = moe.ExpertTable(wl.E, wl.H, wl.I, device)
+        self.path = moe.PATH_AUTO if path is None else path
         offs, stride = synth.expert_blob_layout(wl)
         assert (offs, stride) == moe.ExpertTable.blob_layout(wl.H, wl.I)
-        synth.fill_experts_device(inp, self.table.blob.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        if table is None:
+            table = moe.ExpertTable(wl.E, wl.H, wl.I, device)
+            synth.fill_experts_device(inp, table.blob.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        self.table = table
         if wl.x_dtype == "f32":
             self.x_host = torch.from_numpy(inp.x).pin_memory()
         else:
@@ -175,7 +186,7 @@ class Layer:
 
     def step(self):
         self.moe.forward(self.shape, self.x, self.wr, self.br, self.table.desc, self.shared, self.out, False,
-                         self.ws, ids_out=self.ids, w_out=self.w)
+                         self.ws, ids_out=self.ids, w_out=self.w, path=self.path)
 
     def flush_l2(self):
         # Write a buffer larger than L2, then read another one: the step
@@ -187,13 +198,17 @@ class Layer:
 
     @property
     def decode_path(self) -> bool:
-        return self.wl.T <= self.moe.DECODE_MAX_T or self.wl.x_dtype == "f32"
+        wl, moe = self.wl, self.moe
+        dt = moe.DT_F32 if wl.x_dtype == "f32" else moe.DT_BF16
+        return moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, dt, self.shared is not None, self.path) == moe.PATH_DECODE
 
     def launches_per_step(self) -> int:
         # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
         # shifts), gate/up, down
         if self.decode_path:
-            return 3  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
+            if self.wl.T <= self.moe.DECODE_MAX_T:
+                return 3  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
+            return 8  # router GEMM, top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
         return 7 + (1 if self.shared is not None else 0)
 
     def dominant_stage(self):
@@ -476,12 +491,62 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# -------------------------------------------------------------------- sweep --
+SWEEP_T = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)
+
+
+def sweep(args, device):
+    """Both paths over batch sizes T: uniform routing, H=7168, E=896 experts
+    resident, k=16, I=--sweep-i.  The decode path takes bf16 batches up to
+    DECODE_BATCH_MAX_T tokens and the prefill path any T.  One JSON line per
+    (T, path): tokens/s, the step's algorithmic bytes per second against the
+    measured HBM rate, its FLOP rate, and whether the library's automatic
+    choice takes that path.  Graph replay, L2 flushed before every step
+    (outside the timing)."""
+    import dataclasses
+
+    import mxfp4_routed_expert_moe_gb300 as moe
+    import synth
+    base = synth.WORKLOADS["decode" if args.sweep_i == 1408 else "decode_i1536"]
+    hbm, bf16, _, peak_src = peaks()
+    table = None
+    for T in SWEEP_T:
+        wl = dataclasses.replace(base, name=f"sweep_T{T}_H{base.H}_E{base.E}_k{base.k}_I{base.I}", T=T)
+        paths = [("decode", moe.PATH_DECODE)] if T <= moe.DECODE_BATCH_MAX_T else []
+        paths.append(("prefill", moe.PATH_PREFILL))
+        auto = moe.select_path(T, wl.H, wl.E, wl.I, wl.k)
+        for pname, path in paths:
+            layer = Layer(wl, device, table=table, path=path)
+            table = layer.table
+            layer.step()
+            layer.torch.cuda.synchronize()
+            st = layer.moe.device_status(layer.ws)
+            if st != 0:
+                raise SystemExit(f"T={T} {pname}: device status {st} ({layer.moe.status_string(st)})")
+            n_active = layer.active_experts()
+            step_ms, _ = time_steps(layer, args.steps, max(args.warmup, 3), not args.no_graph)
+            ms = statistics.mean(step_ms)
+            b = layer.algorithmic_bytes_step(n_active)
+            line = {"sweep": wl.name, "T": T, "I": wl.I, "path": pname, "tokens_per_s": T / (ms / 1000.0),
+                    "ms_per_step": ms, "active_experts": n_active, "step_bytes": b,
+                    "weight_gbps": b / (ms / 1000.0) / 1e9, "frac_hbm": b / (ms / 1000.0) / 1e9 / hbm,
+                    "tflops": layer.flops_step() / (ms / 1000.0) / 1e12, "steps": args.steps, "auto": path == auto,
+                    "peak_source": peak_src, "cuda_graph": not args.no_graph}
+            print(json.dumps(line), flush=True)
+            del layer
+
+
 # --------------------------------------------------------------------- main --
 def main():
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         reference_arm(args, rank, world)
+        return
+    if args.sweep:
+        import torch
+        torch.cuda.set_device(0)
+        sweep(args, "cuda:0")
         return
     import torch
     if world > 1:

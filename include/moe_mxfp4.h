@@ -70,8 +70,9 @@
  *     used by two calls that may run concurrently.
  *   - Limits: 1 <= T <= 65536, 32 <= H <= 16384, 32 <= I <= 8192, H % 32 ==
  *     I % 32 == 0, 1 <= k <= min(E, 32), k * (I/32) <= 1024, E <= 65536.
- *     fp32 activations are accepted on the decode path (T <= 64); the prefill
- *     path takes bf16 activations.
+ *     The decode path takes fp32 or bf16 activations for T <= 64 and bf16
+ *     activations up to T = MOE_DECODE_BATCH_MAX_T; the prefill path takes
+ *     bf16 activations.
  */
 #ifndef MOE_MXFP4_H
 #define MOE_MXFP4_H
@@ -100,14 +101,32 @@ typedef enum {
 /* Activation element types. */
 typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 
-/* Expert execution path. */
+/* Expert execution path.
+ *   decode:  the experts' weights stream once through shared memory; gate/up
+ *            on warp tensor cores (bf16 x) or CUDA cores (fp32 x), down on
+ *            CUDA cores, the k outputs of a token combined in slot order.
+ *            T <= MOE_DECODE_MAX_T (the router and top-k then run as one
+ *            GEMV plus a prologue of the gate/up kernel), or bf16 x and
+ *            T <= MOE_DECODE_BATCH_MAX_T (routed with the tiled router GEMM).
+ *   prefill: grouped MXFP4 GEMM on tcgen05 tensor cores, bf16 x; the only
+ *            path with the shared expert.
+ *   auto:    the prefill path when a shared expert is given; else decode for
+ *            T <= MOE_DECODE_MAX_T or fp32 x; else decode while the batch has
+ *            at most MOE_DECODE_AUTO_PAIRS_PER_EXPERT routed pairs per expert
+ *            (T * k <= that * E) and T <= MOE_DECODE_BATCH_MAX_T; else
+ *            prefill.  The bound is the measured crossover of the two paths
+ *            on GB300: below it the decode path's single pass over the
+ *            active experts' weights is faster than the tensor-core GEMMs,
+ *            whose per-tile cost needs many tokens per expert. */
 typedef enum {
-  MOE_PATH_AUTO = 0,    /* decode for T <= 64 or fp32 activations, else prefill */
-  MOE_PATH_DECODE = 1,  /* weight-streaming MXFP4 GEMV on CUDA cores (T <= 64) */
-  MOE_PATH_PREFILL = 2  /* grouped MXFP4 GEMM on tcgen05 tensor cores (bf16 x) */
+  MOE_PATH_AUTO = 0,
+  MOE_PATH_DECODE = 1,
+  MOE_PATH_PREFILL = 2
 } moe_path;
 
 #define MOE_DECODE_MAX_T 64
+#define MOE_DECODE_BATCH_MAX_T 1024
+#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 7
 
 typedef struct { const uint8_t* q; const uint8_t* s; } moe_mx_mat;   /* see above */
 typedef struct { moe_mx_mat gate, up, down; } moe_expert;            /* six tensors */
@@ -116,6 +135,14 @@ typedef struct { int32_t T, H, E, I, k; } moe_shape;
 
 /* MOE_ABI_VERSION of the loaded library. */
 uint32_t moe_abi_version(void);
+
+/* The path a call with this shape, activation type, shared expert (0 / 1)
+ * and `path` argument runs, without running it: *path_out receives
+ * MOE_PATH_DECODE or MOE_PATH_PREFILL.  Returns the status the call would
+ * return for these arguments before launching (MOE_ERR_INVALID_ARG for a bad
+ * shape, enum or null path_out; MOE_ERR_UNSUPPORTED when the requested path
+ * cannot take them).  Host only; no CUDA call. */
+int moe_select_path(const moe_shape* shape, int x_dtype, int has_shared, int path, int* path_out);
 
 /* Static English text for a status code (never NULL). */
 const char* moe_status_string(int status);

@@ -30,12 +30,14 @@ DT_BF16 = 1
 PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_PREFILL = 2
-DECODE_MAX_T = 64
+DECODE_MAX_T = 64                  # MOE_DECODE_MAX_T
+DECODE_BATCH_MAX_T = 1024          # MOE_DECODE_BATCH_MAX_T
+DECODE_AUTO_PAIRS_PER_EXPERT = 7   # MOE_DECODE_AUTO_PAIRS_PER_EXPERT
 
 # Every symbol the header declares (checked by the tests against the .so).
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_route", "moe_mxfp4_experts",
            "moe_forward", "moe_device_status", "moe_profile_events", "moe_forward_static_scratch",
-           "moe_wait_selftest")
+           "moe_wait_selftest", "moe_select_path")
 STATIC_SCRATCH_BYTES = 8 << 20
 
 STAGE_ROUTE, STAGE_GATEUP, STAGE_DOWN, STAGE_COMBINE, STAGE_PF_GATEUP, STAGE_PF_DOWN = 1, 2, 3, 4, 5, 6
@@ -82,6 +84,7 @@ def lib():
             L.moe_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
             L.moe_profile_events.argtypes = [i32, vp, vp]
             L.moe_wait_selftest.argtypes = [ctypes.c_longlong, vp, P(ctypes.c_int)]
+            L.moe_select_path.argtypes = [P(Shape), i32, i32, i32, P(ctypes.c_int)]
             L.moe_forward_static_scratch.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp,
                                                      i32, vp, vp]
             _LIB = L
@@ -102,6 +105,16 @@ def shape(T, H, E, I, k) -> Shape:
 
 def workspace_bytes(T, H, E, I, k) -> int:
     return int(lib().moe_workspace_bytes(ctypes.byref(Shape(T, H, E, I, k))))
+
+
+def select_path(T, H, E, I, k, x_dtype=DT_BF16, shared=False, path=PATH_AUTO) -> int:
+    """moe_select_path: the path (PATH_DECODE or PATH_PREFILL) a call with
+    this shape runs; raises MoeError where the call would fail before
+    launching."""
+    out = ctypes.c_int(-1)
+    _check(lib().moe_select_path(ctypes.byref(Shape(T, H, E, I, k)), int(x_dtype), int(bool(shared)), int(path),
+                                 ctypes.byref(out)), "moe_select_path")
+    return int(out.value)
 
 
 def _ptr(t):

@@ -36,17 +36,31 @@ int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-bool decode_experts_supported(const moe_shape* s) {
-  // Decode gate/up keeps one block column per thread (H <= 8192); down keeps
-  // one block column per thread in groups (I <= 12288 already implied).
-  return s->T <= kDecodeMaxT && s->H <= 8192;
+bool decode_experts_supported(const moe_shape* s, int x_dtype) {
+  // Up to 64 tokens: every decode kernel family (decode gate/up keeps one
+  // block column per thread, H <= 8192).  Larger bf16 batches: the staged
+  // kernels only.
+  if (s->T <= kDecodeMaxT) return s->H <= 8192;
+  return x_dtype == MOE_DT_BF16 && decode_batch_supported(s->T, s->H, s->E, s->I, s->k);
 }
 
-// Resolve MOE_PATH_AUTO and check the chosen path's limits.
-int resolve_path(const moe_shape* s, int x_dtype, int path, int* out) {
-  if (path == MOE_PATH_AUTO) path = (s->T <= kDecodeMaxT || x_dtype == MOE_DT_F32) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+// Resolve MOE_PATH_AUTO (the rule is stated with moe_path in the header) and
+// check the chosen path's limits.
+int resolve_path(const moe_shape* s, int x_dtype, bool has_shared, int path, int* out) {
+  if (path == MOE_PATH_AUTO) {
+    const bool prefill_ok = x_dtype == MOE_DT_BF16 && prefill_supported(s->H, s->I);
+    if (has_shared && prefill_ok)
+      path = MOE_PATH_PREFILL;
+    else if (s->T <= kDecodeMaxT || x_dtype == MOE_DT_F32)
+      path = MOE_PATH_DECODE;
+    else if ((int64_t)s->T * s->k <= (int64_t)MOE_DECODE_AUTO_PAIRS_PER_EXPERT * s->E &&
+             decode_experts_supported(s, x_dtype))
+      path = MOE_PATH_DECODE;
+    else
+      path = MOE_PATH_PREFILL;
+  }
   if (path == MOE_PATH_DECODE) {
-    if (!decode_experts_supported(s)) return MOE_ERR_UNSUPPORTED;
+    if (!decode_experts_supported(s, x_dtype)) return MOE_ERR_UNSUPPORTED;
   } else if (path == MOE_PATH_PREFILL) {
     if (x_dtype != MOE_DT_BF16 || !prefill_supported(s->H, s->I)) return MOE_ERR_UNSUPPORTED;
   } else {
@@ -177,6 +191,17 @@ extern "C" {
 
 uint32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
+int moe_select_path(const moe_shape* shape, int x_dtype, int has_shared, int path, int* path_out) {
+  int st = validate_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!path_out || (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16)) return MOE_ERR_INVALID_ARG;
+  int rpath;
+  if ((st = resolve_path(shape, x_dtype, has_shared != 0, path, &rpath)) != MOE_OK) return st;
+  if (rpath == MOE_PATH_DECODE && has_shared) return MOE_ERR_UNSUPPORTED;
+  *path_out = rpath;
+  return MOE_OK;
+}
+
 const char* moe_status_string(int status) {
   switch (status) {
     case MOE_OK: return "ok";
@@ -224,13 +249,17 @@ int moe_mxfp4_experts(const moe_shape* shape, const void* x, int x_dtype, const 
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(experts, 8) || !aligned(ids, 4) || !aligned(w, 4))
     return MOE_ERR_INVALID_ARG;
   int rpath;
-  if ((st = resolve_path(shape, x_dtype, path, &rpath)) != MOE_OK) return st;
+  if ((st = resolve_path(shape, x_dtype, false, path, &rpath)) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   const Ws L = ws_layout(*shape, ws);
   if ((st = cuda_status(cudaMemsetAsync(L.hdr, 0, sizeof(WsHeader), s))) != MOE_OK) return st;
   BucketParams b = bucket_params(shape, ids, nullptr, nullptr, L);
   if (offsets) {
     if ((st = cuda_status(launch_plan_from_offsets(b, offsets, s))) != MOE_OK) return st;
+    // The kernels read a checked copy of the caller's pair list.
+    if ((st = cuda_status(launch_copy_pairs(sorted_idx, L.sorted, shape->T * shape->k, L.hdr, s))) != MOE_OK)
+      return st;
+    sorted_idx = L.sorted;
   } else {
     if ((st = cuda_status(launch_bucket_from_ids(b, s))) != MOE_OK) return st;
     offsets = L.offsets;
@@ -255,7 +284,7 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
                  !aligned(shared->up, 16) || !aligned(shared->down, 16)))
     return MOE_ERR_INVALID_ARG;
   int rpath;
-  if ((st = resolve_path(shape, x_dtype, path, &rpath)) != MOE_OK) return st;
+  if ((st = resolve_path(shape, x_dtype, shared != nullptr, path, &rpath)) != MOE_OK) return st;
   if (rpath == MOE_PATH_DECODE && shared) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   const Ws L = ws_layout(*shape, ws);

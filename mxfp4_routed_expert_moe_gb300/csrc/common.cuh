@@ -12,6 +12,7 @@
 namespace moe {
 
 constexpr int kDecodeMaxT = MOE_DECODE_MAX_T;
+constexpr int kDecodeBatchMaxT = MOE_DECODE_BATCH_MAX_T;
 constexpr int kMaxK = 32;
 constexpr int kNumSMs = 152;  // GB300; launch code queries the device instead
 
@@ -78,7 +79,8 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.act_pref_dn = (int32_t*)take((E + 1) * 4);
   ws.xh = (uint16_t*)take(T * H * 2);
   ws.xscale = (float*)take(T * 4);
-  const size_t Td = T < (size_t)kDecodeMaxT ? T : (size_t)kDecodeMaxT;
+  // Tokens the decode path may take for this shape (0: it cannot).
+  const size_t Td = T <= (size_t)kDecodeBatchMaxT ? T : 0;
   // h: fp32 for the decode path (Td*k rows), fp16 for the prefill path (T*k rows).
   const size_t h_dec = Td * k * I * 4, h_pf = (T * k + T) * I * 2;
   ws.h = (void*)take(h_dec > h_pf ? h_dec : h_pf);

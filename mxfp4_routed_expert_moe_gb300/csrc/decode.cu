@@ -17,6 +17,8 @@
 //     token's result does not depend on the batch;
 //   * the k expert outputs of a token are combined in slot order ([Deltafin's
 //     custom compiled runtime, "The native build"]: ordered reduction).
+#include <string.h>
+
 #include <utility>
 
 #include "async.cuh"
@@ -306,6 +308,16 @@ __global__ void k_dec_combine(ExpertParams p) {
   }
 }
 
+static cudaError_t launch_decode_combine(const ExpertParams& p, cudaStream_t s) {
+  const int64_t n4 = (int64_t)p.T * (p.H / 4);
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int cgrid = (int)((n4 + 255) / 256 < cap ? (n4 + 255) / 256 : cap);
+  prof_before(MOE_STAGE_COMBINE, s);
+  const cudaError_t err = launch_pdl(k_dec_combine, dim3(cgrid), dim3(256), 0, s, p);
+  prof_after(MOE_STAGE_COMBINE, s);
+  return err;
+}
+
 template <int NT>
 static cudaError_t launch_decode_ldg(const ExpertParams& p, cudaStream_t s) {
   const int nsm = device_sm_count();
@@ -333,13 +345,7 @@ static cudaError_t launch_decode_ldg(const ExpertParams& p, cudaStream_t s) {
   prof_after(MOE_STAGE_DOWN, s);
   if (err != cudaSuccess) return err;
 
-  const int64_t n4 = (int64_t)p.T * (p.H / 4);
-  int cgrid = (int)((n4 + 255) / 256);
-  if (cgrid > nsm * 8) cgrid = nsm * 8;
-  prof_before(MOE_STAGE_COMBINE, s);
-  err = launch_pdl(k_dec_combine, dim3(cgrid), dim3(256), 0, s, p);
-  prof_after(MOE_STAGE_COMBINE, s);
-  return err;
+  return launch_decode_combine(p, s);
 }
 
 // ===================================================== bulk-copy staged path --
@@ -353,9 +359,12 @@ static cudaError_t launch_decode_ldg(const ExpertParams& p, cudaStream_t s) {
 //     results, fed through two mbarrier-guarded slots, so the consumers never
 //     wait on a CTA-wide barrier.
 // Bucket metadata (active experts, their bucket offsets and the routed pairs)
-// is read once per CTA into shared memory.
+// is read once per CTA into shared memory; above kPlanSmemPairs routed pairs
+// (batches of more than 64 tokens) the pair list stays in the workspace,
+// where it only ever holds checked entries (see load_plan).
 constexpr int kMaxStages = 8;
-constexpr int kMaxPairs = kDecodeMaxT * kMaxK;  // routed pairs of a decode batch
+constexpr int kPlanSmemPairs = kDecodeMaxT * kMaxK;
+constexpr int kMaxPairs = kDecodeBatchMaxT * kMaxK;  // routed pairs of a decode batch
 
 struct Ring {
   uint64_t full[kMaxStages];
@@ -366,37 +375,48 @@ struct Ring {
   int abort_flag;
 };
 
-// Bucket metadata in shared memory: per active expert its id, bucket offset,
-// size and the NP tensor pointers the kernel streams (read and checked once
-// per CTA); and every routed pair (sorted by expert).
+// Bucket metadata: per active expert its id, bucket offset, size and the NP
+// tensor pointers the kernel streams (read and checked once per CTA, in
+// shared memory); and every routed pair (sorted by expert): in shared memory
+// (pairs_s) for up to kPlanSmemPairs pairs, else the workspace list.
 struct Plan {
   int U;
   int* ue;
   int* ub0;
   int* un;
-  int* pairs;
+  int* pairs_s;      // shared-memory copy, or null
+  const int* pairs;  // the list the kernel reads: pairs_s or the workspace's
   const uint8_t** ptrs;  // [umax][NP], null for an expert with a bad descriptor
 };
 
+__host__ __device__ inline bool plan_pairs_in_smem(int npairs) { return npairs <= kPlanSmemPairs; }
+
 __host__ __device__ inline size_t plan_smem_bytes(int E, int npairs, int np) {
   const int umax = E < npairs ? E : npairs;
-  return (size_t)(3 * umax + npairs) * 4 + 16 + (size_t)umax * np * 8;
+  const int sp = plan_pairs_in_smem(npairs) ? npairs : 0;
+  return (size_t)(3 * umax + sp) * 4 + 16 + (size_t)umax * np * 8;
 }
 
 __device__ Plan plan_carve(const ExpertParams& p, uint8_t* buf, int np) {
   Plan pl;
   const int npairs = p.T * p.k;
   const int umax = p.E < npairs ? p.E : npairs;
+  const int sp = plan_pairs_in_smem(npairs) ? npairs : 0;
   pl.U = 0;
   pl.ue = reinterpret_cast<int*>(buf);
   pl.ub0 = pl.ue + umax;
   pl.un = pl.ub0 + umax;
-  pl.pairs = pl.un + umax;
-  pl.ptrs = reinterpret_cast<const uint8_t**>((reinterpret_cast<uintptr_t>(pl.pairs + npairs) + 15) & ~(uintptr_t)15);
+  pl.pairs_s = sp ? pl.un + umax : nullptr;
+  pl.pairs = sp ? pl.pairs_s : p.sorted;
+  pl.ptrs = reinterpret_cast<const uint8_t**>((reinterpret_cast<uintptr_t>(pl.un + umax + sp) + 15) & ~(uintptr_t)15);
   return pl;
 }
 
-// Plan from the published route (workspace / caller layout).
+// Plan from the published route (workspace / caller layout).  The pairs are
+// checked on their way into shared memory; a list too long for that is read
+// in place, and the library only passes such a list from its own workspace:
+// built by its bucketing kernels, or a checked copy of the caller's (the
+// experts-only call copies it with k_copy_pairs first).
 __device__ void load_plan(const ExpertParams& p, Plan& pl) {
   pl.U = (int)p.ws.hdr->n_active;
   const int npairs = p.T * p.k;
@@ -407,13 +427,14 @@ __device__ void load_plan(const ExpertParams& p, Plan& pl) {
     pl.ub0[u] = b0;
     pl.un[u] = p.offsets[e + 1] - b0;
   }
+  if (!pl.pairs_s) return;
   for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
     int v = p.sorted[i];
     if (v < 0 || v >= npairs) {
       set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
       v = -1;
     }
-    pl.pairs[i] = v;
+    pl.pairs_s[i] = v;
   }
 }
 
@@ -577,7 +598,7 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
     sp.ue = pl.ue;
     sp.ub0 = pl.ub0;
     sp.un = pl.un;
-    sp.pairs = pl.pairs;
+    sp.pairs = pl.pairs_s;
     route_small(p.rp, reinterpret_cast<char*>(ring_data), sp, blockIdx.x == 0);
     pl.U = sp.U;
     // Generic-proxy writes to the ring must be ordered before the bulk
@@ -913,7 +934,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
   __shared__ Ring rs;
   __shared__ float2 red[2][kGmMaxWarps][kGmRows][kGmCols / 2];
   __shared__ GmRedMeta rmeta[2];
-  __shared__ float xs_s[kDecodeMaxT];
+  __shared__ float xs_s[kDecodeMaxT];  // 2^-sigma of the first 64 tokens (the others: ws.xscale)
   // Per stage, written by the producer with the item: first row, bucket
   // offset and size, and the tokens of the first pass's 8 columns.
   __shared__ int4 imeta[kMaxStages];
@@ -947,13 +968,13 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
   pdl_trigger();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < (H + 31) / 32; i += blockDim.x) p.ws.rowdone[i] = 0u;
-  for (int t = threadIdx.x; t < p.T; t += blockDim.x) xs_s[t] = p.ws.xscale[t];
+  for (int t = threadIdx.x; t < p.T && t < kDecodeMaxT; t += blockDim.x) xs_s[t] = p.ws.xscale[t];
   if (p.fused_route) {
     SmallPlan sp;
     sp.ue = pl.ue;
     sp.ub0 = pl.ub0;
     sp.un = pl.un;
-    sp.pairs = pl.pairs;
+    sp.pairs = pl.pairs_s;
     route_small(p.rp, reinterpret_cast<char*>(ring_data), sp, blockIdx.x == 0);
     pl.U = sp.U;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1056,7 +1077,8 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
         if (col < m.n) {
           const int ent = pl.pairs[m.b0 + col];
           if (ent >= 0) {
-            const float xs = xs_s[ent / k];
+            const int tk = ent / k;
+            const float xs = tk < kDecodeMaxT ? xs_s[tk] : __ldg(&p.ws.xscale[tk]);
             const float g = (i ? gs.y : gs.x) * xs, uu = (i ? us.y : us.x) * xs;
             hout[(size_t)ent * I + h_swz(m.r0 + r)] = silu_f32(g) * uu;
           }
@@ -1174,9 +1196,11 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
 // quarter-warp reads one even and one odd 704-byte row x 4 consecutive 16-byte
 // chunks: 8 distinct bank groups, no conflict.  The warp's sum over its 4
 // block columns is two xor-shuffle steps; the reducer adds the warps in
-// order.  h of the item's first NT pairs is staged by the producer.  When all
-// active experts have written a row tile, the reducer that finished last
-// combines it into out in slot order.
+// order.  h of the item's first NT pairs is staged by the producer.  For up
+// to 64 tokens, when all active experts have written a row tile, the reducer
+// that finished last combines it into out in slot order; larger batches are
+// combined by k_dec_combine after the kernel (the same arithmetic, spread
+// over the whole grid instead of one warp per row tile).
 constexpr int kDnG = 8;                 // row groups
 constexpr int kDnRPG = 8;               // rows per group
 constexpr int kDnRows = kDnG * kDnRPG;  // rows per item
@@ -1277,7 +1301,7 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
         }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rs.red_empty[slot]);
-      if (m.last) {
+      if (m.last && T <= kDecodeMaxT) {
         __threadfence();
         __syncwarp();
         unsigned prev = 0;
@@ -1525,7 +1549,8 @@ static cudaError_t launch_decode_down(const ExpertParams& p, cudaStream_t s, siz
   prof_before(MOE_STAGE_DOWN, s);
   err = launch_pdl(dn, dim3(nsm), dim3(nbI * kDnG + 64), dn_smem, s, p, dn_stages, dn_stage);
   prof_after(MOE_STAGE_DOWN, s);
-  return err;
+  if (err != cudaSuccess || p.T <= kDecodeMaxT) return err;
+  return launch_decode_combine(p, s);
 }
 
 template <int NT>
@@ -1551,6 +1576,14 @@ cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp,
   if (err != cudaSuccess) return err;
   p.fused_route = 0;
   return launch_decode_experts(p, s);
+}
+
+bool decode_batch_supported(int T, int H, int E, int I, int k) {
+  ExpertParams p;
+  memset(&p, 0, sizeof p);
+  p.T = T; p.H = H; p.E = E; p.I = I; p.k = k;
+  p.x_bf16 = 1;
+  return T >= 1 && T <= kDecodeBatchMaxT && H <= 8192 && tma_path_ok<2>(p) && gm_quads_per_warp(p) != 0;
 }
 
 // NT = routed pairs of one expert processed per weight pass.  The choice

@@ -54,8 +54,14 @@ cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s);
 cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s);
 cudaError_t launch_bucket_from_ids(const BucketParams& b, cudaStream_t s);
 cudaError_t launch_plan_from_offsets(const BucketParams& b, const int32_t* offsets, cudaStream_t s);
+// out[i] = in[i] for i < npairs, or -1 (and MOE_ERR_DEVICE_CHECK in hdr) where
+// in[i] is not in [0, npairs).
+cudaError_t launch_copy_pairs(const int32_t* in, int32_t* out, int npairs, WsHeader* hdr, cudaStream_t s);
 
 // decode.cu
+// Whether the staged decode kernels take a bf16 batch of this shape (the
+// decode path of batches above 64 tokens runs only on them).
+bool decode_batch_supported(int T, int H, int E, int I, int k);
 cudaError_t launch_decode_experts(const ExpertParams& p, cudaStream_t s);
 cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s);
 

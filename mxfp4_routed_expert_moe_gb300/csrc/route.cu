@@ -458,6 +458,18 @@ __global__ void k_bucket_scatter(BucketParams p) {
   if (p.sorted_out) p.sorted_out[pos] = i;
 }
 
+// A checked copy of a caller-given pair list (see launch_copy_pairs).
+__global__ void k_copy_pairs(const int32_t* in, int32_t* out, int npairs, WsHeader* hdr) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= npairs) return;
+  int v = in[i];
+  if (v < 0 || v >= npairs) {
+    set_status(hdr, MOE_ERR_DEVICE_CHECK);
+    v = -1;
+  }
+  out[i] = v;
+}
+
 // Plan from a caller-given offsets array: counts, then the same scan.
 // A layout that is not a partition of [0, T*k) (decreasing offsets, or
 // offsets outside that range) is flagged and no expert work is planned.
@@ -505,6 +517,11 @@ cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cu
   k_bucket_count<<<(p.E + 7) / 8, 256, 0, s>>>(b);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   k_bucket_scatter<<<(p.T * p.k + 255) / 256, 256, 0, s>>>(b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_pairs(const int32_t* in, int32_t* out, int npairs, WsHeader* hdr, cudaStream_t s) {
+  k_copy_pairs<<<(npairs + 255) / 256, 256, 0, s>>>(in, out, npairs, hdr);
   return cudaGetLastError();
 }
 

@@ -94,10 +94,14 @@ def test_forward_and_experts_reject_bad_arguments(moe):
     # fp32 activations are not taken by the prefill path.
     rc = L.moe_forward(ctypes.byref(shp), A, 0, A, None, A, None, A, 0, None, None, 2, A, wsb, None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
-    # Decode path limited to 64 tokens.
-    shp2 = moe.shape(65, 256, 8, 128, 2)
+    # Decode path: bf16 batches up to DECODE_BATCH_MAX_T tokens, fp32 up to 64.
+    shp2 = moe.shape(moe.DECODE_BATCH_MAX_T + 1, 256, 8, 128, 2)
     wsb2 = L.moe_workspace_bytes(ctypes.byref(shp2))
     rc = L.moe_forward(ctypes.byref(shp2), A, 1, A, None, A, None, A, 0, None, None, 1, A, wsb2, None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    shp3 = moe.shape(65, 256, 8, 128, 2)
+    wsb3 = L.moe_workspace_bytes(ctypes.byref(shp3))
+    rc = L.moe_forward(ctypes.byref(shp3), A, 0, A, None, A, None, A, 0, None, None, 1, A, wsb3, None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
     # Experts-only: offsets without sorted_idx.
     rc = L.moe_mxfp4_experts(ctypes.byref(shp), A, 1, A, A, A, A, None, A, 0, 0, A, wsb, None)
@@ -117,3 +121,41 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle.c" not in text and "from oracle" not in text, f
                 assert "synth" not in text or f == "build.py" and "synth" not in text, f
+
+
+def test_select_path_rules(moe):
+    """The automatic path choice as the header states it: prefill with a shared
+    expert; decode up to 64 tokens or for fp32 activations; decode for larger
+    bf16 batches while T*k <= DECODE_AUTO_PAIRS_PER_EXPERT * E and T <=
+    DECODE_BATCH_MAX_T; else prefill.  Host only."""
+    D, P = moe.PATH_DECODE, moe.PATH_PREFILL
+    H, E, I, k = 7168, 896, 1408, 16
+    sel = moe.select_path
+    assert sel(1, H, E, I, k) == D
+    assert sel(64, H, E, I, k) == D
+    assert sel(64, H, E, I, k, x_dtype=moe.DT_F32) == D
+    t_max = moe.DECODE_AUTO_PAIRS_PER_EXPERT * E // k  # largest T the rule sends to decode
+    assert t_max <= moe.DECODE_BATCH_MAX_T
+    assert sel(t_max, H, E, I, k) == D
+    assert sel(t_max + 1, H, E, I, k) == P
+    assert sel(4096, H, E, I, k) == P
+    # Few experts: many pairs per expert, the tensor-core path.
+    assert sel(512, H, 64, I, k) == P
+    assert sel(65, H, 64, I, k) == P
+    # Shared expert: prefill at any T (decode has no shared expert).
+    assert sel(1, H, E, I, k, shared=True) == P
+    # Explicit paths.
+    assert sel(512, H, 64, I, k, path=D) == D
+    assert sel(1, H, E, I, k, path=P) == P
+    with pytest.raises(moe.MoeError) as ei:
+        sel(moe.DECODE_BATCH_MAX_T + 1, H, E, I, k, path=D)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as ei:
+        sel(65, H, E, I, k, x_dtype=moe.DT_F32)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as ei:
+        sel(1, H, E, I, k, x_dtype=moe.DT_F32, shared=True)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as ei:
+        sel(0, H, E, I, k)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
