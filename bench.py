@@ -1,7 +1,7 @@
 """Benchmark of the routed MXFP4 MoE layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|wide|prefill|long|decode_i1536|tiny]
+                    [--workload decode|wide|batch256|prefill|long|decode_i1536|tiny]
     python bench.py --sweep [--sweep-i 1408|1536] [--steps K]
 
 A step is one pass of the whole layer (moe_forward: router, top-k, bucketing,

@@ -103,8 +103,9 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 
 /* Expert execution path.
  *   decode:  the experts' weights stream once through shared memory; gate/up
- *            on warp tensor cores (bf16 x) or CUDA cores (fp32 x), down on
- *            CUDA cores, the k outputs of a token combined in slot order.
+ *            on warp tensor cores (bf16 x) or CUDA cores (fp32 x); down on
+ *            CUDA cores up to 64 tokens and on warp tensor cores above; the
+ *            k outputs of a token combined in slot order.
  *            T <= MOE_DECODE_MAX_T (the router and top-k then run as one
  *            GEMV plus a prologue of the gate/up kernel), or bf16 x and
  *            T <= MOE_DECODE_BATCH_MAX_T (routed with the tiled router GEMM).
@@ -126,7 +127,7 @@ typedef enum {
 
 #define MOE_DECODE_MAX_T 64
 #define MOE_DECODE_BATCH_MAX_T 1024
-#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 7
+#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 12
 
 typedef struct { const uint8_t* q; const uint8_t* s; } moe_mx_mat;   /* see above */
 typedef struct { moe_mx_mat gate, up, down; } moe_expert;            /* six tensors */
@@ -176,9 +177,11 @@ int moe_route(const moe_shape* shape, const void* x, int x_dtype, const float* w
  *             rebuilt in ws from ids)
  *   out       [T][H] fp32
  *   path      moe_path
- * The decode path sums the k expert outputs of a token in slot order and is
- * bitwise independent of the other tokens in the batch; the prefill path adds
- * them with fp32 atomics (order not fixed).
+ * The decode path sums the k expert outputs of a token in slot order, and a
+ * token's result is bitwise independent of the other tokens in the batch
+ * among batches of 1 to 64 tokens, and among batches of 65 to
+ * MOE_DECODE_BATCH_MAX_T tokens (the two ranges run different down kernels);
+ * the prefill path adds them with fp32 atomics (order not fixed).
  * [deltafin, "The techniques that bought the 82x": fused MXFP4 dequant+GEMV;
  *  Deltafin's custom compiled runtime, "The native build": ordered reduction.] */
 int moe_mxfp4_experts(const moe_shape* shape, const void* x, int x_dtype, const moe_expert* experts,

@@ -1441,6 +1441,365 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
   }
 }
 
+// ------------------------------------- down + combine on warp tensor cores --
+// Decode batches above 64 tokens (after k_dec_gateup_mma), I % 128 == 0.
+// (Up to 64 tokens k_dec_down_tma runs: it is faster at one token, and one
+// kernel serves that whole range so that a token's result does not depend
+// on the batch.)  Item =
+// (active expert u, 64 rows of Wd) = four m16n8k16 A tiles; the MMA's 8
+// columns are 8 routed pairs (one pass).  Consumer warp w owns the K-blocks
+// [4w, 4w+4) of I for every item and keeps the pass columns' h for them in
+// registers as two f16 terms, hi + lo, of h * 2^sigma (about 22 significant
+// bits; sigma per pair and warp puts the largest magnitude of that range in
+// [2^14, 2^15)); the sum is multiplied by 2^-sigma after the warp's blocks.
+// Rows are copied in pairs (or one by one when I/2 is a multiple of 128
+// bytes) with 16 bytes of padding per copy, which puts the 8 rows a fragment
+// read touches at 8 distinct 16-byte bank groups.  Two reducer warps (one per
+// hand-off slot) add the warps' partial sums in order and write y; the
+// slot-ordered combine into out is the next launch (k_dec_combine, spread
+// over the whole GPU).
+constexpr int kDmRows = 64;                // rows of Wd per item
+constexpr int kDmTiles = kDmRows / 16;     // MMA row tiles per item
+constexpr int kDmMaxWarps = 12;            // consumer warps (I <= 1536)
+
+struct DmRedMeta {
+  int r0;    // first row of the item
+  int b0;    // bucket offset of the expert
+  int n;     // routed pairs of the expert
+  int pass;  // first pair of this pass
+};
+
+constexpr int kDmRpcOverride = 0;
+__host__ __device__ inline int dm_rows_per_copy(int I) {
+  return kDmRpcOverride ? kDmRpcOverride : ((I / 2) % 128 == 64 ? 2 : 1);
+}
+__host__ __device__ inline uint32_t dm_group_stride(int I) {
+  return (uint32_t)(dm_rows_per_copy(I) * (I / 2) + 16);
+}
+__host__ __device__ inline uint32_t dm_row_off(int r, int I) {
+  const int rpc = dm_rows_per_copy(I);
+  return (uint32_t)(r / rpc) * dm_group_stride(I) + (uint32_t)(r % rpc) * (uint32_t)(I / 2);
+}
+__host__ __device__ inline uint32_t dm_scale_off(int I) {
+  return (uint32_t)(kDmRows / dm_rows_per_copy(I)) * dm_group_stride(I);
+}
+__host__ __device__ inline uint32_t dm_stage_bytes(int I) {
+  return (dm_scale_off(I) + (uint32_t)kDmRows * (uint32_t)(I / 32) + 127u) & ~127u;
+}
+
+// One K-block of one 16-row tile against the hi and lo activation terms.
+template <bool PLAIN, int J>
+__device__ __forceinline__ void dm_block(const uint32_t wg, const uint32_t wu, const uint4 hb, const uint4 lb,
+                                         uint32_t sg, uint32_t su, float (&acc)[4]) {
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t a0 = e2m1x2_f16x2(wg, 0), a1 = e2m1x2_f16x2(wu, 0), a2 = e2m1x2_f16x2(wg, 1),
+                 a3 = e2m1x2_f16x2(wu, 1);
+  const uint32_t a4 = e2m1x2_f16x2(wg, 2), a5 = e2m1x2_f16x2(wu, 2), a6 = e2m1x2_f16x2(wg, 3),
+                 a7 = e2m1x2_f16x2(wu, 3);
+  float d[4];
+  mma_f16_16816(d, a0, a1, a2, a3, hb.x, hb.y, zero);
+  mma_f16_16816(d, a4, a5, a6, a7, hb.z, hb.w, d);
+  mma_f16_16816(d, a0, a1, a2, a3, lb.x, lb.y, d);
+  mma_f16_16816(d, a4, a5, a6, a7, lb.z, lb.w, d);
+  float fg, fu;
+  if (PLAIN) {
+    fg = __uint_as_float(((sg >> (8 * J)) & 0xFFu) << 23);
+    fu = __uint_as_float(((su >> (8 * J)) & 0xFFu) << 23);
+  } else {
+    fg = e8m0_f32((sg >> (8 * J)) & 0xFFu);
+    fu = e8m0_f32((su >> (8 * J)) & 0xFFu);
+  }
+  acc[0] = fmaf(d[0], fg, acc[0]);
+  acc[1] = fmaf(d[1], fg, acc[1]);
+  acc[2] = fmaf(d[2], fu, acc[2]);
+  acc[3] = fmaf(d[3], fu, acc[3]);
+}
+
+// The four blocks of one tile: rows at ag (row g) and au (row g + 8), scale
+// words sg / su.
+template <bool PLAIN>
+__device__ __forceinline__ void dm_tile(const uint8_t* ag, const uint8_t* au, const uint4 (&hb)[4],
+                                        const uint4 (&lb)[4], uint32_t sg, uint32_t su, float (&acc)[4]) {
+  dm_block<PLAIN, 0>(lds32(ag), lds32(au), hb[0], lb[0], sg, su, acc);
+  dm_block<PLAIN, 1>(lds32(ag + 16), lds32(au + 16), hb[1], lb[1], sg, su, acc);
+  dm_block<PLAIN, 2>(lds32(ag + 32), lds32(au + 32), hb[2], lb[2], sg, su, acc);
+  dm_block<PLAIN, 3>(lds32(ag + 48), lds32(au + 48), hb[3], lb[3], sg, su, acc);
+}
+
+__global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
+    k_dec_down_mma(ExpertParams p, int stages, uint32_t stage_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ Ring rs;
+  __shared__ float2 red[2][kDmMaxWarps][kDmTiles][16][kGmCols / 2];
+  __shared__ DmRedMeta rmeta[2];
+  const int H = p.H, I = p.I;
+  const int nbI = I / 32;
+  const int W = nbI / 4;  // consumer warps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t qrow = (uint32_t)(I / 2);
+  const int rpc = dm_rows_per_copy(I);
+  const uint32_t gstride = dm_group_stride(I), sc_off = dm_scale_off(I);
+  uint8_t* ring_data = smem;
+  Plan pl = plan_carve(p, smem + (size_t)stages * stage_bytes, 2);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&rs.full[s], 1);
+      mbar_init(&rs.empty[s], W);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&rs.red_full[s], W);
+      mbar_init(&rs.red_empty[s], 1);
+    }
+    rs.abort_flag = 0;
+    mbar_init_fence();
+  }
+  pdl_wait();
+  pdl_trigger();
+  load_plan(p, pl);
+  __syncthreads();
+  plan_cache_ptrs(p, pl, 1);
+  __syncthreads();
+  const int tiles = H / kDmRows;
+  const int n_items = pl.U * tiles;
+  const int beg = (int)((long long)n_items * blockIdx.x / gridDim.x);
+  const int n_mine = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x) - beg;
+  const float* hin = reinterpret_cast<const float*>(p.ws.h);
+
+  if (warp == W) {  // producer: the lanes issue one item's copies
+    int issued_use[kMaxStages];
+    for (int i = 0; i < kMaxStages; ++i) issued_use[i] = -1;
+    bool ok = true;
+    const int ncopy = kDmRows / rpc;
+    for (int it = 0;; ++it) {
+      const int s = it % stages, use = it / stages;
+      const int item = it < n_mine ? beg + it : -1;
+      if (lane == 0) {
+        if (use > 0 && !mbar_wait(&rs.empty[s], (use - 1) & 1)) ok = false;
+        if (ok && *(volatile int*)&rs.abort_flag) ok = false;
+        if (ok) rs.item[s] = item;
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      uint64_t* bar = &rs.full[s];
+      if (item < 0) {
+        if (lane == 0) mbar_arrive(bar);
+        break;
+      }
+      const int u = item / tiles, rt = item % tiles;
+      const uint8_t* const* pp = pl.ptrs + u * 2;
+      if (!pp[0]) {  // bad descriptor: flagged in the plan, not read
+        if (lane == 0) mbar_arrive(bar);
+        continue;
+      }
+      const size_t r0 = (size_t)rt * kDmRows;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)kDmRows * qrow + (uint32_t)kDmRows * (uint32_t)nbI);
+        issued_use[s] = use;
+      }
+      __syncwarp();
+      uint8_t* st = ring_data + (size_t)s * stage_bytes;
+      for (int c = lane; c < ncopy; c += 32)
+        bulk_g2s(st + (size_t)c * gstride, pp[0] + (r0 + (size_t)c * rpc) * qrow, (uint32_t)rpc * qrow, bar);
+      if (lane == 31) bulk_g2s(st + sc_off, pp[1] + r0 * nbI, (uint32_t)(kDmRows * nbI), bar);
+    }
+    if (!ok && lane == 0) {
+      set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+      rs.abort_flag = 1;
+      for (int s = 0; s < stages; ++s)
+        if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
+    }
+    return;
+  }
+
+  if (warp == W + 1 || warp == W + 2) {  // reducers: reducer r takes the passes that use slot r
+    const int slot = warp - (W + 1);
+    for (int j = 0;; ++j) {
+      if (!mbar_wait(&rs.red_full[slot], j & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        break;
+      }
+      const DmRedMeta m = rmeta[slot];
+      if (m.r0 < 0) break;
+      // Lane: outputs o = lane + 32 q = (tile, row, column pair cp), columns
+      // 2cp and 2cp+1 of the pass; the warps' partial sums are added in warp
+      // order (all loads issued together).
+      constexpr int kOut = kDmTiles * 16 * (kGmCols / 2) / 32;
+      float2 sums[kOut];
+#pragma unroll
+      for (int q = 0; q < kOut; ++q) {
+        const int o = lane + 32 * q;
+        const int tile = o / (16 * (kGmCols / 2)), rem = o % (16 * (kGmCols / 2));
+        const int r = rem / (kGmCols / 2), cp = rem % (kGmCols / 2);
+        float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kDmMaxWarps; ++w)
+          if (w < W) {
+            const float2 v = red[slot][w][tile][r][cp];
+            sum.x += v.x;
+            sum.y += v.y;
+          }
+        sums[q] = sum;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_empty[slot]);
+#pragma unroll
+      for (int q = 0; q < kOut; ++q) {
+        const int o = lane + 32 * q;
+        const int tile = o / (16 * (kGmCols / 2)), rem = o % (16 * (kGmCols / 2));
+        const int r = rem / (kGmCols / 2), cp = rem % (kGmCols / 2);
+        const float2 sum = sums[q];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int col = m.pass + 2 * cp + i;
+          if (col < m.n) {
+            const int ent = pl.pairs[m.b0 + col];
+            if (ent >= 0) p.ws.y[(size_t)ent * H + m.r0 + 16 * tile + r] = i ? sum.y : sum.x;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // consumers
+  const int g = lane >> 2, t = lane & 3;
+  const int kb0 = warp * 4;  // first K-block of this warp
+  uint4 hb[4], lb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) hb[j] = lb[j] = make_uint4(0u, 0u, 0u, 0u);
+  float cs[2] = {1.f, 1.f};  // 2^-sigma of columns 2t and 2t+1
+  int hcur = -2;             // pair whose h is in hb / lb (-1: zeros)
+  int pc = 0;
+  bool dead = false;
+  for (int it = 0; !dead; ++it) {
+    const int s = it % stages;
+    if (!mbar_wait(&rs.full[s], (it / stages) & 1)) {
+      set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+      rs.abort_flag = 1;
+      break;
+    }
+    const int item = rs.item[s];
+    if (item < 0) break;
+    const int u = item / tiles, rt = item % tiles;
+    const int b0 = pl.ub0[u], n = pl.un[u];
+    const uint8_t* st = ring_data + (size_t)s * stage_bytes;
+    const uint8_t* scp = st + sc_off + (size_t)kb0;  // + row * nbI
+    const int npass = n > 0 ? (n + kGmCols - 1) / kGmCols : 1;
+    for (int pi = 0; pi < npass; ++pi) {
+      const int pass = pi * kGmCols;
+      const int pe = pass + g < n ? pl.pairs[b0 + pass + g] : -1;
+      if (__any_sync(0xFFFFFFFFu, pe != hcur)) {
+        // h of pair pe (column g), elements 8t..8t+7 of the warp's 4 blocks;
+        // h is stored block-interleaved (h_swz): the 4 floats of chunk c of
+        // block b sit at float (b/4)*128 + c*16 + (b%4)*4.
+        float v[4][8];
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int b = kb0 + j;
+          if (pe >= 0) {
+            const float* src = hin + (size_t)pe * I + (size_t)(b >> 2) * 128 + (b & 3) * 4;
+            const float4 x0 = *reinterpret_cast<const float4*>(src + (2 * t) * 16);
+            const float4 x1 = *reinterpret_cast<const float4*>(src + (2 * t + 1) * 16);
+            v[j][0] = x0.x; v[j][1] = x0.y; v[j][2] = x0.z; v[j][3] = x0.w;
+            v[j][4] = x1.x; v[j][5] = x1.y; v[j][6] = x1.z; v[j][7] = x1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[j][e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[j][e]));
+        }
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        int sig = 0;
+        if (m > 0.f) sig = 14 - ((int)((__float_as_uint(m) >> 23) & 0xFF) - 127);
+        sig = sig > 100 ? 100 : (sig < -100 ? -100 : sig);
+        const float up = __int_as_float((sig + 127) << 23);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = v[j][2 * e] * up, b = v[j][2 * e + 1] * up;
+            const __half2 h2 = __floats2half2_rn(a, b);
+            const float2 hf = __half22float2(h2);
+            const __half2 l2 = __floats2half2_rn(a - hf.x, b - hf.y);
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+          }
+          hb[j] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          lb[j] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        const float inv = __int_as_float((127 - sig) << 23);
+        cs[0] = __shfl_sync(0xFFFFFFFFu, inv, 4 * (2 * t));
+        cs[1] = __shfl_sync(0xFFFFFFFFu, inv, 4 * (2 * t + 1));
+        hcur = pe;
+      }
+      float acc[kDmTiles][4];
+#pragma unroll
+      for (int tl = 0; tl < kDmTiles; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
+      uint32_t spec = 0u;
+#pragma unroll
+      for (int tl = 0; tl < kDmTiles; ++tl) {
+        const int rg = 16 * tl + g;
+        const uint32_t sg = lds32(scp + (size_t)rg * nbI), su = lds32(scp + (size_t)(rg + 8) * nbI);
+        spec |= e8m0_special4(sg) | e8m0_special4(su);
+        dm_tile<true>(st + dm_row_off(rg, I) + kb0 * 16 + 4 * t, st + dm_row_off(rg + 8, I) + kb0 * 16 + 4 * t, hb,
+                      lb, sg, su, acc[tl]);
+      }
+      // Scale codes 0 and 255 need the exact conversion: the pass is redone
+      // (warp-uniform: the MMAs need all lanes).
+      if (__any_sync(0xFFFFFFFFu, (spec & 0x80808080u) != 0u)) {
+#pragma unroll 1
+        for (int tl = 0; tl < kDmTiles; ++tl) {
+          const int rg = 16 * tl + g;
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
+          dm_tile<false>(st + dm_row_off(rg, I) + kb0 * 16 + 4 * t, st + dm_row_off(rg + 8, I) + kb0 * 16 + 4 * t,
+                         hb, lb, lds32(scp + (size_t)rg * nbI), lds32(scp + (size_t)(rg + 8) * nbI), a);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[tl][i] = a[i];
+        }
+      }
+      const int slot = pc & 1;
+      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+        dead = true;
+        break;
+      }
+#pragma unroll
+      for (int tl = 0; tl < kDmTiles; ++tl) {
+        red[slot][warp][tl][g][t] = make_float2(acc[tl][0] * cs[0], acc[tl][1] * cs[1]);
+        red[slot][warp][tl][g + 8][t] = make_float2(acc[tl][2] * cs[0], acc[tl][3] * cs[1]);
+      }
+      if (warp == 0 && lane == 0) {
+        DmRedMeta m;
+        m.r0 = rt * kDmRows;
+        m.b0 = b0;
+        m.n = n;
+        m.pass = pass;
+        rmeta[slot] = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+      ++pc;
+    }
+    if (dead) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rs.empty[s]);
+  }
+  // Tell both reducers there is no more work.
+  for (int e = 0; e < 2; ++e, ++pc) {
+    const int slot = pc & 1;
+    if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
+    if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rs.red_full[slot]);
+  }
+}
+
 template <int NT>
 static bool tma_path_ok(const ExpertParams& p) {
   const int R = kGuRowsNT / NT;
@@ -1494,6 +1853,36 @@ static cudaError_t launch_gateup_mma(const ExpertParams& p, cudaStream_t s, size
   return err;
 }
 
+// Tensor-core down (after the tensor-core gate/up, batches above 64 tokens):
+// I % 128 == 0, at most kDmMaxWarps consumer warps, H % 64 == 0.
+static bool dm_ok(const ExpertParams& p) {
+  const int nbI = p.I / 32;
+  return p.I % 128 == 0 && nbI / 4 >= 1 && nbI / 4 <= kDmMaxWarps && p.H % kDmRows == 0;
+}
+
+static cudaError_t launch_down_mma(const ExpertParams& p, cudaStream_t s, size_t smem_max) {
+  const int W = p.I / 128;
+  const int threads = (W + 3) * 32;
+  auto kern = k_dec_down_mma;
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, (const void*)kern);
+  if (err != cudaSuccess) return err;
+  const size_t cap = (size_t)227 * 1024 - fa.sharedSizeBytes;
+  smem_max = smem_max < cap ? smem_max : cap;
+  const size_t plan = plan_smem_bytes(p.E, p.T * p.k, 2);
+  const uint32_t stage = dm_stage_bytes(p.I);
+  int stages = (int)((smem_max - plan) / stage);
+  stages = stages > kMaxStages ? kMaxStages : stages;
+  if (stages < 2) return cudaErrorNotSupported;
+  const size_t smem = (size_t)stages * stage + plan;
+  if ((err = ensure_smem_attr((const void*)kern, smem)) != cudaSuccess) return err;
+  prof_before(MOE_STAGE_DOWN, s);
+  err = launch_pdl(kern, dim3(device_sm_count()), dim3(threads), smem, s, p, stages, stage);
+  prof_after(MOE_STAGE_DOWN, s);
+  if (err != cudaSuccess) return err;
+  return launch_decode_combine(p, s);
+}
+
 template <int NT>
 static cudaError_t launch_decode_tma(const ExpertParams& p, cudaStream_t s) {
   constexpr int R = kGuRowsNT / NT;
@@ -1506,6 +1895,7 @@ static cudaError_t launch_decode_tma(const ExpertParams& p, cudaStream_t s) {
     err = qw == 1 ? launch_gateup_mma<1>(p, s, smem_max)
                   : (qw == 2 ? launch_gateup_mma<2>(p, s, smem_max) : launch_gateup_mma<4>(p, s, smem_max));
     if (err != cudaSuccess) return err;
+    if (p.T > kDecodeMaxT && dm_ok(p)) return launch_down_mma(p, s, (size_t)227 * 1024);
     return launch_decode_down<NT>(p, s, smem_max);
   }
   const int nbH = p.H / 32;

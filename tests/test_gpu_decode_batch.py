@@ -1,8 +1,8 @@
 """GPU parity of the decode path on batches above 64 tokens (bf16
 activations): routed by the tiled router GEMM and the bucketing kernels, then
-the staged decode kernels (tensor-core gate/up, bulk-copy down) and the
-slot-ordered combine as a kernel of its own.  Above 2048 routed pairs the
-kernels read the pair list from the workspace instead of shared memory."""
+the staged decode kernels (tensor-core gate/up and down) and the
+slot-ordered combine as a kernel of its own.  Above 2048 routed pairs the kernels read the pair list
+from the workspace instead of shared memory."""
 import numpy as np
 import pytest
 
@@ -107,10 +107,11 @@ def test_decode_batch_experts_calls_match_forward():
     assert t.equal(out_b, out_f)
 
 
-def test_decode_batch_invariance_across_combine_variants():
+def test_decode_batch_invariance():
     """Given the same routes, a token's decode output is bitwise the same in a
-    300-token batch (workspace pair list, combine kernel), a 150-token batch
-    and a 64-token batch (shared-memory pair list, fused combine)."""
+    300-token batch (workspace pair list), a 150-token and an 80-token batch
+    (shared-memory pair list): above 64 tokens one set of kernels serves
+    every batch size."""
     t = torch()
     wl = synth.Workload("invariance", 300, 512, 32, 8, 256)
     inp = synth.make_inputs(wl, seed=21)
@@ -118,7 +119,7 @@ def test_decode_batch_invariance_across_combine_variants():
     out_all, ids, w = L.forward(path=1)
     t.cuda.synchronize()
     assert L.status() == 0
-    for lo, n in ((0, 64), (100, 150)):
+    for lo, n in ((100, 150), (7, 80)):
         shp = L.moe.shape(n, wl.H, wl.E, wl.I, wl.k)
         ws = t.empty(L.moe.workspace_bytes(n, wl.H, wl.E, wl.I, wl.k), dtype=t.uint8, device="cuda")
         out = t.zeros((n, wl.H), dtype=t.float32, device="cuda")
