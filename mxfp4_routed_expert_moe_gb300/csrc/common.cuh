@@ -48,12 +48,29 @@ struct Ws {
   void* h;              // [T*k][I] fp32 (decode) or [T*k + T][I] fp16 (prefill; rows
                         // T*k.. hold the shared expert's h)
   int32_t* shsig;       // [2I + H] row shifts of the bf16 shared expert (gate, up, down)
-  float* y;             // [T*k][H] fp32 (decode, T <= 64)
+  float* y;             // [T*k][H] fp32 (decode, T <= 1024)
+  float2* rpart;        // [S][T][E] router partial sums of the S K-splits (S > 1 only)
   uint32_t* rowdone;    // [ceil(H/32)] per-row-tile completion counters
   size_t total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Splits of the contraction of the router GEMM (64 experts x 64 tokens per
+// CTA) for batches above 64 tokens (smaller ones keep their workspace size;
+// their decode route is the GEMV): enough CTAs for about three per SM on 152
+// SMs, each split at least 256 long, at most 16.  A function of the shape
+// only, so that the workspace size needs no device query and a shape always
+// sums in the same order.
+__host__ __device__ inline int router_splits(int T, int E, int H) {
+  if (T <= kDecodeMaxT) return 1;
+  const int tiles = ((E + 63) / 64) * ((T + 63) / 64);
+  int s = (456 + tiles - 1) / tiles;
+  const int smax = H / 256;
+  s = s < smax ? s : smax;
+  s = s < 16 ? s : 16;
+  return s < 1 ? 1 : s;
+}
 
 // Layout of the workspace for a shape; pointers are offsets from `base`.
 inline Ws ws_layout(const moe_shape& s, void* base) {
@@ -87,6 +104,8 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.shsig = (int32_t*)take((2 * I + H) * 4);
   ws.y = (float*)take(Td * k * H * 4);
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
+  const size_t S = (size_t)router_splits(s.T, s.E, s.H);
+  ws.rpart = (float2*)take(S > 1 ? S * T * E * 8 : 0);
   ws.total = off;
   return ws;
 }

@@ -240,7 +240,9 @@ cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
 // 16-wide K step is staged through double-buffered shared memory (vector
 // loads for the next step are in flight while this one is computed), summed
 // in fp32 and added into a double-float accumulator (hi, lo).  Also clears
-// the per-expert token masks.
+// the per-expert token masks.  Small batches have few tiles: the contraction
+// is then split over blockIdx.z (router_splits), each split writes its
+// (hi, lo) partial sums, and k_router_reduce adds them in split order.
 constexpr int kGmTT = 64, kGmTE = 64, kGmK = 16;
 
 template <bool XBF16>
@@ -251,10 +253,14 @@ __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
   const int T = p.T, H = p.H, E = p.E;
   const int t0 = blockIdx.y * TT, e0 = blockIdx.x * TE;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  // This CTA's part of the contraction: K steps [kbeg, kend).
+  const int nsplit = gridDim.z, steps = (H / KS + nsplit - 1) / nsplit;
+  const int kbeg = min(H, (int)blockIdx.z * steps * KS), kend = min(H, kbeg + steps * KS);
   {
     const size_t nmask = (size_t)E * ((T + 31) / 32);
-    const size_t gtid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-    const size_t gsz = (size_t)gridDim.x * gridDim.y * blockDim.x;
+    const size_t gtid =
+        (((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t gsz = (size_t)gridDim.x * gridDim.y * gridDim.z * blockDim.x;
     for (size_t i = gtid; i < nmask; i += gsz) p.ws.mask[i] = 0u;
   }
   float4 wreg[NW];
@@ -311,12 +317,14 @@ __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < NE; ++j) { ah[i][j] = 0.f; al[i][j] = 0.f; }
-  gload(0);
-  sstore(0);
+  if (kbeg < kend) {
+    gload(kbeg);
+    sstore(0);
+  }
   __syncthreads();
   int buf = 0;
-  for (int kk = 0; kk < H; kk += KS, buf ^= 1) {
-    const bool more = kk + KS < H;
+  for (int kk = kbeg; kk < kend; kk += KS, buf ^= 1) {
+    const bool more = kk + KS < kend;
     if (more) gload(kk + KS);
     float acc[4][NE];
 #pragma unroll
@@ -353,11 +361,30 @@ __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
     for (int j = 0; j < NE; ++j) {
       const int e = e0 + tx * NE + j;
       if (e < E) {
-        float sh, sl;
-        df_add(ah[i][j], al[i][j], p.br ? p.br[e] : 0.f, 0.f, sh, sl);
-        p.ws.logits[(size_t)t * E + e] = make_float2(sh, sl);
+        if (nsplit > 1) {
+          p.ws.rpart[((size_t)blockIdx.z * T + t) * E + e] = make_float2(ah[i][j], al[i][j]);
+        } else {
+          float sh, sl;
+          df_add(ah[i][j], al[i][j], p.br ? p.br[e] : 0.f, 0.f, sh, sl);
+          p.ws.logits[(size_t)t * E + e] = make_float2(sh, sl);
+        }
       }
     }
+  }
+}
+
+// logits = the S partial sums added in split order, then the bias.
+__global__ void __launch_bounds__(256) k_router_reduce(RouteParams p, int nsplit) {
+  const size_t n = (size_t)p.T * p.E;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    float sh = 0.f, sl = 0.f;
+    for (int z = 0; z < nsplit; ++z) {
+      const float2 v = p.ws.rpart[(size_t)z * n + i];
+      df_add(sh, sl, v.x, v.y, sh, sl);
+    }
+    const int e = (int)(i % p.E);
+    df_add(sh, sl, p.br ? p.br[e] : 0.f, 0.f, sh, sl);
+    p.ws.logits[i] = make_float2(sh, sl);
   }
 }
 
@@ -500,14 +527,22 @@ __global__ void __launch_bounds__(1024) k_plan_from_offsets(BucketParams p, cons
 cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cudaStream_t s) {
   // 64-expert x 64-token tiles: 80 registers, three CTAs per SM (a 128-expert
   // tile needs 137 registers and one CTA per SM, and was slower).
-  const dim3 g1((p.E + kGmTE - 1) / kGmTE, (p.T + kGmTT - 1) / kGmTT);
+  const int nsplit = router_splits(p.T, p.E, p.H);
+  const dim3 g1((p.E + kGmTE - 1) / kGmTE, (p.T + kGmTT - 1) / kGmTT, nsplit);
   prof_before(MOE_STAGE_ROUTE, s);
   if (p.x_bf16)
     k_router_gemm<true><<<g1, 256, 0, s>>>(p);
   else
     k_router_gemm<false><<<g1, 256, 0, s>>>(p);
-  prof_after(MOE_STAGE_ROUTE, s);
   cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess && nsplit > 1) {
+    const size_t n = (size_t)p.T * p.E;
+    const size_t cap = (size_t)device_sm_count() * 8;
+    const int grid = (int)((n + 255) / 256 < cap ? (n + 255) / 256 : cap);
+    k_router_reduce<<<grid, 256, 0, s>>>(p, nsplit);
+    err = cudaGetLastError();
+  }
+  prof_after(MOE_STAGE_ROUTE, s);
   if (err != cudaSuccess) return err;
   const size_t smem = (size_t)8 * p.E * 8;
   err = ensure_smem_attr((const void*)k_topk, smem);

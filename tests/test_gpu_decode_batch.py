@@ -150,3 +150,21 @@ def test_decode_batch_bad_pair_entry_is_flagged():
     _, same = check_route(inp, ids.cpu().numpy(), w.cpu().numpy())
     toks = np.nonzero(same)[0]
     check_out(out.cpu().numpy()[toks], oracle_out(inp, toks), "after bad pair entry")
+
+
+def test_router_split_contraction_routes():
+    """The router GEMM splits its contraction when the batch has few tiles
+    (here 16 splits: 100 tokens, 64 experts, H = 4096) and adds the splits'
+    double-float partial sums in order; routes, weights and buckets match the
+    oracle, with a per-expert bias."""
+    from harness import check_buckets
+    wl = synth.Workload("split_router", 100, 4096, 64, 8, 128)
+    inp = synth.make_inputs(wl, seed=8)
+    inp.br = (np.arange(wl.E, dtype=np.float32) % 7 - 3.0) * 0.05
+    L = DeviceLayer(inp)
+    ids, w, off, srt = L.route()
+    torch().cuda.synchronize()
+    assert L.status() == 0
+    ids, w, off, srt = (a.cpu().numpy() for a in (ids, w, off, srt))
+    check_route(inp, ids, w)
+    check_buckets(ids, off, srt, wl.E)
