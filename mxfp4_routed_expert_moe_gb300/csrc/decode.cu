@@ -29,11 +29,13 @@ namespace moe {
 
 // Dot product of one MX block (16 bytes q, scale s) with NT activation blocks
 // of 32 fp32 values each, accumulated into acc[nt] (scaled by 2^(s-127)).
+// Even and odd elements accumulate separately (.x and .y), each lane of the
+// packed FMA one fmaf.
 template <int NT>
 __device__ __forceinline__ void mx_block_dot(const uint4 q, uint32_t s, const float (&xr)[NT][32], float (&acc)[NT]) {
-  float pe[NT], po[NT];
+  float2 pp[NT];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) { pe[n] = 0.f; po[n] = 0.f; }
+  for (int n = 0; n < NT; ++n) pp[n] = make_float2(0.f, 0.f);
   const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int wd = 0; wd < 4; ++wd) {
@@ -42,15 +44,12 @@ __device__ __forceinline__ void mx_block_dot(const uint4 q, uint32_t s, const fl
       const float2 f = f16x2_f32x2(e2m1x2_f16x2(words[wd], b));
       const int c = wd * 8 + b * 2;
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        pe[n] = fmaf(f.x, xr[n][c], pe[n]);
-        po[n] = fmaf(f.y, xr[n][c + 1], po[n]);
-      }
+      for (int n = 0; n < NT; ++n) pp[n] = __ffma2_rn(f, make_float2(xr[n][c], xr[n][c + 1]), pp[n]);
     }
   }
   const float sc = e8m0_f32(s);
 #pragma unroll
-  for (int n = 0; n < NT; ++n) acc[n] = fmaf(pe[n] + po[n], sc, acc[n]);
+  for (int n = 0; n < NT; ++n) acc[n] = fmaf(pp[n].x + pp[n].y, sc, acc[n]);
 }
 
 template <bool XBF16>

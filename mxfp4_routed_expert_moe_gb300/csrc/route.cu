@@ -326,30 +326,35 @@ __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
   for (int kk = kbeg; kk < kend; kk += KS, buf ^= 1) {
     const bool more = kk + KS < kend;
     if (more) gload(kk + KS);
-    float acc[4][NE];
+    // The chunk's fp32 sums, two experts per packed FMA (each lane one fmaf).
+    float2 acc[4][NE / 2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < NE; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < NE / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
       const float4 a4 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 4]);
       const float a[4] = {a4.x, a4.y, a4.z, a4.w};
-      float b[NE];
+      float2 b[NE / 2];
 #pragma unroll
       for (int j = 0; j < NE; j += 4) {
         const float4 b4 = *reinterpret_cast<const float4*>(&ws_[buf][k][tx * NE + j]);
-        b[j] = b4.x; b[j + 1] = b4.y; b[j + 2] = b4.z; b[j + 3] = b4.w;
+        b[j / 2] = make_float2(b4.x, b4.y);
+        b[j / 2 + 1] = make_float2(b4.z, b4.w);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < NE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < NE / 2; ++j) acc[i][j] = __ffma2_rn(make_float2(a[i], a[i]), b[j], acc[i][j]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < NE; ++j) df_add_f(ah[i][j], al[i][j], acc[i][j]);
+      for (int j = 0; j < NE / 2; ++j) {
+        df_add_f(ah[i][2 * j], al[i][2 * j], acc[i][j].x);
+        df_add_f(ah[i][2 * j + 1], al[i][2 * j + 1], acc[i][j].y);
+      }
     if (more) sstore(buf ^ 1);
     __syncthreads();
   }
