@@ -206,10 +206,21 @@ class Layer:
         # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
         # shifts), gate/up, down
         if self.decode_path:
+            # shared expert: x->fp16, its row shifts, and the two prefill GEMMs on its tiles alone
+            sh = 4 if self.shared is not None else 0
             if self.wl.T <= self.moe.DECODE_MAX_T:
-                return 3  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
-            return 8  # router GEMM, top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
-        return 7 + (1 if self.shared is not None else 0)
+                return 3 + sh  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
+            # router GEMM (+ split reduction), top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
+            return 8 + sh + (1 if self._router_splits() > 1 else 0)
+        return 7 + (1 if self.shared is not None else 0) + (1 if self._router_splits() > 1 else 0)
+
+    def _router_splits(self) -> int:
+        """Splits of the router GEMM's contraction (the library's rule)."""
+        wl = self.wl
+        if wl.T <= self.moe.DECODE_MAX_T:
+            return 1
+        tiles = ((wl.E + 63) // 64) * ((wl.T + 63) // 64)
+        return max(1, min(-(-456 // tiles), wl.H // 256, 16))
 
     def dominant_stage(self):
         return self.moe.STAGE_GATEUP if self.decode_path else self.moe.STAGE_PF_GATEUP

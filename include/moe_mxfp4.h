@@ -109,13 +109,14 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
  *            T <= MOE_DECODE_MAX_T (the router and top-k then run as one
  *            GEMV plus a prologue of the gate/up kernel), or bf16 x and
  *            T <= MOE_DECODE_BATCH_MAX_T (routed with the tiled router GEMM).
- *   prefill: grouped MXFP4 GEMM on tcgen05 tensor cores, bf16 x; the only
- *            path with the shared expert.
- *   auto:    the prefill path when a shared expert is given; else decode for
- *            T <= MOE_DECODE_MAX_T or fp32 x; else decode while the batch has
- *            at most MOE_DECODE_AUTO_PAIRS_PER_EXPERT routed pairs per expert
- *            (T * k <= that * E) and T <= MOE_DECODE_BATCH_MAX_T; else
- *            prefill.  The bound is the measured crossover of the two paths
+ *            A shared expert (bf16 x) runs after the routed experts on the
+ *            prefill path's GEMM kernels, alone, adding into out.
+ *   prefill: grouped MXFP4 GEMM on tcgen05 tensor cores, bf16 x, with the
+ *            shared expert's tiles after the routed ones.
+ *   auto:    decode for T <= MOE_DECODE_MAX_T or fp32 x; else decode while
+ *            the batch has at most MOE_DECODE_AUTO_PAIRS_PER_EXPERT routed
+ *            pairs per expert (T * k <= that * E) and T <=
+ *            MOE_DECODE_BATCH_MAX_T; else prefill.  The bound is the measured crossover of the two paths
  *            on GB300: below it the decode path's single pass over the
  *            active experts' weights is faster than the tensor-core GEMMs,
  *            whose per-tile cost needs many tokens per expert. */

@@ -48,10 +48,7 @@ bool decode_experts_supported(const moe_shape* s, int x_dtype) {
 // check the chosen path's limits.
 int resolve_path(const moe_shape* s, int x_dtype, bool has_shared, int path, int* out) {
   if (path == MOE_PATH_AUTO) {
-    const bool prefill_ok = x_dtype == MOE_DT_BF16 && prefill_supported(s->H, s->I);
-    if (has_shared && prefill_ok)
-      path = MOE_PATH_PREFILL;
-    else if (s->T <= kDecodeMaxT || x_dtype == MOE_DT_F32)
+    if (s->T <= kDecodeMaxT || x_dtype == MOE_DT_F32)
       path = MOE_PATH_DECODE;
     else if ((int64_t)s->T * s->k <= (int64_t)MOE_DECODE_AUTO_PAIRS_PER_EXPERT * s->E &&
              decode_experts_supported(s, x_dtype))
@@ -61,6 +58,8 @@ int resolve_path(const moe_shape* s, int x_dtype, bool has_shared, int path, int
   }
   if (path == MOE_PATH_DECODE) {
     if (!decode_experts_supported(s, x_dtype)) return MOE_ERR_UNSUPPORTED;
+    // The decode path runs a shared expert on the prefill kernels.
+    if (has_shared && (x_dtype != MOE_DT_BF16 || !prefill_supported(s->H, s->I))) return MOE_ERR_UNSUPPORTED;
   } else if (path == MOE_PATH_PREFILL) {
     if (x_dtype != MOE_DT_BF16 || !prefill_supported(s->H, s->I)) return MOE_ERR_UNSUPPORTED;
   } else {
@@ -197,7 +196,6 @@ int moe_select_path(const moe_shape* shape, int x_dtype, int has_shared, int pat
   if (!path_out || (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16)) return MOE_ERR_INVALID_ARG;
   int rpath;
   if ((st = resolve_path(shape, x_dtype, has_shared != 0, path, &rpath)) != MOE_OK) return st;
-  if (rpath == MOE_PATH_DECODE && has_shared) return MOE_ERR_UNSUPPORTED;
   *path_out = rpath;
   return MOE_OK;
 }
@@ -285,7 +283,6 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
     return MOE_ERR_INVALID_ARG;
   int rpath;
   if ((st = resolve_path(shape, x_dtype, shared != nullptr, path, &rpath)) != MOE_OK) return st;
-  if (rpath == MOE_PATH_DECODE && shared) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   const Ws L = ws_layout(*shape, ws);
   int32_t* ids = ids_out ? ids_out : L.ids;
@@ -294,7 +291,14 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
   const ExpertParams p = expert_params(shape, x, x_dtype, experts, ids, w, L.offsets, L.sorted, out, accumulate, shared, L);
   if (rpath == MOE_PATH_DECODE) {
     const RouteParams rp = route_params(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L);
-    return cuda_status(launch_decode_forward(rp, bucket_params(shape, ids, nullptr, nullptr, L), p, s));
+    st = cuda_status(launch_decode_forward(rp, bucket_params(shape, ids, nullptr, nullptr, L), p, s));
+    if (st != MOE_OK || !shared) return st;
+    // The shared expert: the prefill GEMM kernels with no routed items (the
+    // active-expert count cleared), adding its output into out.
+    if ((st = cuda_status(cudaMemsetAsync(&L.hdr->n_active, 0, sizeof(uint32_t), s))) != MOE_OK) return st;
+    ExpertParams ps = p;
+    ps.accumulate = 1;
+    return cuda_status(launch_prefill_experts(ps, s));
   }
   if ((st = do_route(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L, false, s)) != MOE_OK) return st;
   return run_experts(p, rpath, s);

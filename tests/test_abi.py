@@ -124,10 +124,10 @@ def test_product_path_has_no_oracle_dependency():
 
 
 def test_select_path_rules(moe):
-    """The automatic path choice as the header states it: prefill with a shared
-    expert; decode up to 64 tokens or for fp32 activations; decode for larger
-    bf16 batches while T*k <= DECODE_AUTO_PAIRS_PER_EXPERT * E and T <=
-    DECODE_BATCH_MAX_T; else prefill.  Host only."""
+    """The automatic path choice as the header states it: decode up to 64
+    tokens or for fp32 activations; decode for larger bf16 batches while
+    T*k <= DECODE_AUTO_PAIRS_PER_EXPERT * E and T <= DECODE_BATCH_MAX_T; else
+    prefill.  Host only."""
     D, P = moe.PATH_DECODE, moe.PATH_PREFILL
     H, E, I, k = 7168, 896, 1408, 16
     sel = moe.select_path
@@ -142,8 +142,14 @@ def test_select_path_rules(moe):
     # Few experts: many pairs per expert, the tensor-core path.
     assert sel(512, H, 64, I, k) == P
     assert sel(65, H, 64, I, k) == P
-    # Shared expert: prefill at any T (decode has no shared expert).
-    assert sel(1, H, E, I, k, shared=True) == P
+    # A shared expert does not change the choice: the decode path runs it on
+    # the prefill kernels after the routed experts (bf16, H and I % 128 == 0).
+    assert sel(1, H, E, I, k, shared=True) == D
+    assert sel(512, H, E, I, k, shared=True) == D
+    assert sel(4096, H, E, I, k, shared=True) == P
+    with pytest.raises(moe.MoeError) as ei:
+        sel(1, 7168 + 32, E, I, k, shared=True)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
     # Explicit paths.
     assert sel(512, H, 64, I, k, path=D) == D
     assert sel(1, H, E, I, k, path=P) == P

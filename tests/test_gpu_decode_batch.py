@@ -168,3 +168,36 @@ def test_router_split_contraction_routes():
     ids, w, off, srt = (a.cpu().numpy() for a in (ids, w, off, srt))
     check_route(inp, ids, w)
     check_buckets(ids, off, srt, wl.E)
+
+
+@pytest.mark.parametrize("T", [5, 200])
+def test_decode_path_with_shared_expert(T):
+    """A bf16 shared expert on the decode path (run after the routed experts
+    on the prefill kernels, alone) matches the oracle, and agrees with the
+    prefill path, which takes it with the routed tiles."""
+    wl = synth.Workload(f"shared_T{T}", T, 256, 16, 4, 128, shared=True)
+    inp = synth.make_inputs(wl, seed=4)
+    L, out, ids, w = _check_forward(inp, wl.name, path=1)
+    o2, _, _ = L.forward(path=2)
+    torch().cuda.synchronize()
+    assert L.status() == 0
+    a, b = out.cpu().numpy().astype(np.float64), o2.cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-3
+
+
+def test_prefill_workload_auto_takes_decode_path_with_shared_expert():
+    """The 512-token layer with the shared expert: the automatic choice runs
+    the routed experts on the decode path and the shared expert on the
+    prefill kernels; sampled tokens against the oracle."""
+    import mxfp4_routed_expert_moe_gb300 as moe
+    wl = synth.WORKLOADS["prefill"]
+    assert moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, shared=True) == moe.PATH_DECODE
+    inp = synth.make_inputs(wl)
+    L = DeviceLayer(inp)
+    out, ids, w = L.forward()
+    torch().cuda.synchronize()
+    assert L.status() == 0
+    _, same = check_route(inp, ids.cpu().numpy(), w.cpu().numpy())
+    toks = np.nonzero(same)[0]
+    toks = toks[np.linspace(0, toks.size - 1, 3).astype(int)]
+    check_out(out.cpu().numpy()[toks], oracle_out(inp, toks), "prefill workload, decode path + shared")
