@@ -880,10 +880,13 @@ __device__ __forceinline__ void gm_block(const uint8_t* ag, const uint8_t* au, c
     fg = e8m0_f32((sg >> (8 * J)) & 0xFFu);
     fu = e8m0_f32((su >> (8 * J)) & 0xFFu);
   }
-  acc[0] = fmaf(d[0], fg, acc[0]);
-  acc[1] = fmaf(d[1], fg, acc[1]);
-  acc[2] = fmaf(d[2], fu, acc[2]);
-  acc[3] = fmaf(d[3], fu, acc[3]);
+  // acc += d * scale, two rows' fmaf per packed FMA.
+  const float2 a01 = __ffma2_rn(make_float2(d[0], d[1]), make_float2(fg, fg), make_float2(acc[0], acc[1]));
+  const float2 a23 = __ffma2_rn(make_float2(d[2], d[3]), make_float2(fu, fu), make_float2(acc[2], acc[3]));
+  acc[0] = a01.x;
+  acc[1] = a01.y;
+  acc[2] = a23.x;
+  acc[3] = a23.y;
 }
 
 // One pass over the warp's QW quads of K-blocks with the scales taken as plain

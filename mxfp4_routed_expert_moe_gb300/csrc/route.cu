@@ -234,6 +234,24 @@ cudaError_t launch_route_decode(const RouteParams& p, cudaStream_t s) {
   return launch_pdl(k_route_small, dim3(1), dim3(256), smem, s, p);
 }
 
+// df_add_f on two accumulators at once: (h0, l0) += p.x and (h1, l1) += p.y,
+// each lane the same two-sum (a - b written as fma(b, -1, a), exact like the
+// subtraction).
+__device__ __forceinline__ void df_add_f2(float& h0, float& h1, float& l0, float& l1, float2 p) {
+  const float2 m1 = make_float2(-1.f, -1.f);
+  const float2 a = make_float2(h0, h1);
+  const float2 s = __fadd2_rn(a, p);
+  const float2 bp = __ffma2_rn(a, m1, s);           // s - a
+  const float2 t = __ffma2_rn(bp, m1, s);           // s - bp
+  const float2 e1 = __ffma2_rn(t, m1, a);           // a - (s - bp)
+  const float2 e2 = __ffma2_rn(bp, m1, p);          // p - bp
+  const float2 lo = __fadd2_rn(make_float2(l0, l1), __fadd2_rn(e1, e2));
+  h0 = s.x;
+  h1 = s.y;
+  l0 = lo.x;
+  l1 = lo.y;
+}
+
 // ------------------------------------------------------- prefill router GEMM --
 // s = x Wr^T (+ b) in fp32 on CUDA cores.  A CTA computes 64 experts x 64
 // tokens; thread (tx, ty) of 16 x 16 holds 4 experts x 4 tokens.  Each
@@ -351,10 +369,7 @@ __global__ void __launch_bounds__(256) k_router_gemm(RouteParams p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < NE / 2; ++j) {
-        df_add_f(ah[i][2 * j], al[i][2 * j], acc[i][j].x);
-        df_add_f(ah[i][2 * j + 1], al[i][2 * j + 1], acc[i][j].y);
-      }
+      for (int j = 0; j < NE / 2; ++j) df_add_f2(ah[i][2 * j], ah[i][2 * j + 1], al[i][2 * j], al[i][2 * j + 1], acc[i][j]);
     if (more) sstore(buf ^ 1);
     __syncthreads();
   }
