@@ -1,4 +1,6 @@
-// decode.cu — weight-streaming MXFP4 expert kernels for small batches (T <= 64).
+// decode.cu — weight-streaming MXFP4 expert kernels: decode steps of up to 64
+// tokens, and bf16 batches of up to 1024 tokens whose experts each have few
+// routed pairs.
 //
 // The fused MXFP4 dequant+GEMV of [deltafin, "The techniques that bought the
 // 82x"] (16-entry table lookup, E8M0 scale as a power of two on the fp32
@@ -11,10 +13,15 @@
 //   * gate/up with bf16 activations (k_dec_gateup_mma) multiplies on warp
 //     tensor cores: m16n8k16 MMAs over 8 gate + 8 up rows against 8 routed
 //     pairs, the activations carried as f16 with a per-token power-of-two
-//     shift so that every product is exact; the other decode kernels sum
-//     exact products on CUDA cores, one MX block column per thread;
-//   * partial sums are added across lanes and warps in a fixed order, so each
-//     token's result does not depend on the batch;
+//     shift so that every product is exact;
+//   * down runs on CUDA cores up to 64 tokens (k_dec_down_tma: exact
+//     products, one MX block column per thread) and on warp tensor cores for
+//     larger batches (k_dec_down_mma: 8 routed pairs per pass); the
+//     fp32-activation gate/up and the register-streaming kernels also sum
+//     exact products on CUDA cores;
+//   * partial sums are added across lanes and warps in a fixed order, so a
+//     token's result does not depend on the batch, among batches of up to 64
+//     tokens and among larger ones;
 //   * the k expert outputs of a token are combined in slot order ([Deltafin's
 //     custom compiled runtime, "The native build"]: ordered reduction).
 #include <string.h>
