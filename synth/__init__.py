@@ -203,6 +203,10 @@ WORKLOADS = {
     # Small-footprint case of the decode kernels for profiler captures: 32
     # experts resident (515 MB, above the 129 MB L2), 16 of them routed.
     "decode_e32": Workload("decode_T1_H7168_E32_k16_I1408", 1, 7168, 32, 16, 1408),
+    # Small-footprint case of the batched decode kernels for profiler
+    # captures: 80 tokens over 256 experts resident (4.1 GB), ~5 routed pairs
+    # per active expert, as in a 256-token batch of the full layer.
+    "batch80_e256": Workload("batch_decode_T80_H7168_E256_k16_I1408", 80, 7168, 256, 16, 1408),
     # Small-footprint case of the prefill kernels for profiler captures: 64
     # experts resident (1.03 GB), 512 tokens, ~128 tokens per expert.
     "prefill_e64": Workload("prefill_T512_H7168_E64_k16_I1408", 512, 7168, 64, 16, 1408),
