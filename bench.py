@@ -12,6 +12,14 @@ line (rank 0).  For N > 1 (torchrun) every rank runs an independent replica
 of the workload on its own GPU (the layer has no exchange step here), the
 time is the max over ranks and `value` counts the tokens of all ranks.
 
+With the default workload the same line also carries `prefill_long`: the
+4096-token Zipf prefill (tensor-core grouped GEMMs) timed the same way, with
+its own roofline, parity, cpu_baseline and e2e figures.
+
+Before anything is timed, the layer's output on a few sampled tokens is
+checked against the fp64 oracle (ids, route weights, outputs within the
+parity tolerances); a mismatch prints the line with "value": null and exits 1.
+
 --impl reference times the fp64 CPU oracle (the reference arm) on the host
 cores, each step a bounded sample of the same workload.
 """
@@ -44,6 +52,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
+    ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"],
+                    help="expert path of the workload (default: the library's own choice)")
+    ap.add_argument("--no-prefill-leg", action="store_true",
+                    help="with the default 1-token decode workload, skip the 4096-token prefill leg")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
@@ -404,10 +416,87 @@ def traffic_from_profiles(kernel: str, workload: str):
 
 
 # ------------------------------------------------------------------- oracle --
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def sample_tokens(inp, n):
+    """Up to n tokens spread over the batch whose oracle route has no near-tie:
+    every gap between consecutive scores among the first k+1 is at least twice
+    the error bound of the library's router arithmetic (products summed in fp32
+    in chunks of at most 16, chunk sums carried in double-float)."""
+    import numpy as np
+
+    import oracle
+    wl = inp.wl
+    u = 2.0 ** -24
+    gam = 16 * u / (1 - 16 * u) + 2.0 ** -40
+    absw = np.abs(inp.wr).astype(np.float64)
+    toks = []
+    for i in range(8 * n + 16):
+        tok = (i * 7919) % wl.T
+        if tok in toks:
+            continue
+        sc = oracle.router_logits(inp.x[[tok]], inp.wr, inp.br)
+        _, _, margin = oracle.topk(sc, wl.k)
+        mag = absw @ np.abs(inp.x_f32[tok]).astype(np.float64)
+        if inp.br is not None:
+            mag = mag + np.abs(inp.br.astype(np.float64))
+        if wl.k >= wl.E or margin[0] >= 2.0 * gam * 1.01 * float(mag.max()):
+            toks.append(tok)
+        if len(toks) == n:
+            break
+    return toks or [0]
+
+
+def parity_check(layer, ntok):
+    """The output of the layer's last step on sampled tokens against the fp64
+    oracle: ids equal, route weights within 1e-6, outputs within rel-L2 1e-3
+    and max-abs 1e-2 * rms (the parity tolerances)."""
+    import numpy as np
+
+    import oracle
+    inp, wl = layer.inp, layer.wl
+    toks = sample_tokens(inp, ntok)
+    t0 = time.perf_counter()
+    ref, rids, rw = oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array(toks),
+                                      shared=inp.shared, nthreads=oracle.default_threads())
+    dt = time.perf_counter() - t0
+    got = layer.out.cpu().numpy()[toks].astype(np.float64)
+    ids = layer.ids.cpu().numpy()[toks]
+    w = layer.w.cpu().numpy()[toks]
+    ids_ok = bool(np.array_equal(ids, rids))
+    dw = float(np.abs(w.astype(np.float64) - rw).max()) if ids_ok else None
+    err = got - ref
+    rel = float(np.linalg.norm(err) / max(float(np.linalg.norm(ref)), 1e-300))
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    mx = float(np.abs(err).max()) / rms if rms > 0 else float("inf")
+    ok = bool(ids_ok and dw <= 1e-6 and rel <= 1e-3 and mx <= 1e-2)
+    return {"ok": ok, "when": "before the timed region", "tokens": [int(t) for t in toks], "ids_equal": ids_ok,
+            "max_abs_dw": dw, "rel_l2": rel, "max_abs_over_rms": mx, "oracle_seconds": round(dt, 3)}
+
+
 def cpu_baseline(layer, seconds: float):
-    """The fp64 oracle on the host cores on a bounded sample of the workload:
-    whole tokens of the layer, repeated until `seconds` of CPU time elapsed.
-    Also returns the oracle-vs-GPU error on the sampled tokens."""
+    """The fp64 oracle as it stands on the host cores, on a bounded sample of
+    the workload: whole tokens of the layer, repeated until `seconds` elapsed
+    (at most 64); then the same sample timed again with every expert already
+    materialised on the host (the first pass includes their generation).  For
+    workloads of at most 64 tokens, also one token on one thread."""
     import numpy as np
 
     import oracle
@@ -415,31 +504,32 @@ def cpu_baseline(layer, seconds: float):
     threads = oracle.default_threads()
     tokens = []
     t0 = time.perf_counter()
-    outs = []
     i = 0
     while True:
         tok = (i * 7919) % wl.T
-        out, ids, w = oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array([tok]),
-                                        shared=inp.shared, nthreads=threads)
+        oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array([tok]), shared=inp.shared,
+                          nthreads=threads)
         tokens.append(tok)
-        outs.append(out[0])
         i += 1
         if time.perf_counter() - t0 >= seconds or i >= 64:
             break
-    # Exclude the on-demand host generation of expert weights from the timing:
-    # time the same sample again with every expert already materialised.
     t0 = time.perf_counter()
     for tok in tokens:
         oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array([tok]), shared=inp.shared,
                           nthreads=threads)
     dt = time.perf_counter() - t0
-    got = layer.out.cpu().numpy().astype(np.float64)
-    ref = np.stack(outs)
-    err = got[tokens] - ref
-    rel = float(np.linalg.norm(err) / np.linalg.norm(ref))
-    return {"value": len(tokens) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(tokens)} token(s) of {wl.name} through the whole layer (fp64, {threads} threads)",
-            "seconds": round(dt, 3)}, {"tokens": len(tokens), "rel_l2_vs_oracle": rel}
+    cb = {"value": len(tokens) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+          "sample": f"{len(tokens)} token(s) of {wl.name} through the whole layer (fp64, {threads} threads)",
+          "seconds": round(dt, 3), "cpu_model": cpu_model()}
+    if wl.T <= 64:
+        t0 = time.perf_counter()
+        oracle.moe_tokens(inp.x, inp.wr, inp.br, inp.expert, wl.E, wl.I, wl.k, np.array([tokens[0]]),
+                          shared=inp.shared, nthreads=1)
+        d1 = time.perf_counter() - t0
+        cb["single_thread"] = {"value": 1.0 / d1, "unit": "tokens/s", "cores": 1,
+                               "sample": f"1 token of {wl.name} through the whole layer (fp64, 1 thread)",
+                               "seconds": round(d1, 3)}
+    return cb
 
 
 def reference_arm(args, rank, world):
@@ -548,6 +638,116 @@ def sweep(args, device):
 
 
 # --------------------------------------------------------------------- main --
+PATHS = {"auto": None, "decode": 1, "prefill": 2}
+
+
+def step_stats(step_ms):
+    q = sorted(step_ms)
+
+    def pct(p):
+        return q[min(len(q) - 1, max(0, int(round(p / 100.0 * (len(q) - 1)))))]
+
+    return {"n": len(q), "mean": statistics.mean(q), "median": statistics.median(q), "p10": pct(10), "p90": pct(90),
+            "min": q[0], "max": q[-1]}
+
+
+def all_ranks_ok(ok: bool, world: int, device: str) -> bool:
+    if world <= 1:
+        return ok
+    import torch
+    t = torch.tensor([1 if ok else 0], dtype=torch.int32, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MIN)
+    return bool(t.item())
+
+
+def measure(layer, args, rank, world, local, device, steps, cpu_seconds, parity_tokens):
+    """One workload: parity on sampled tokens, then `steps` timed steps (L2
+    flushed before each), the dominant kernel's roofline, the per-stage
+    breakdown, the end-to-end figure and (rank 0) the oracle's CPU baseline.
+    Returns (fields, parity); fields is None when parity failed."""
+    torch = layer.torch
+    wl = layer.wl
+    layer.step()
+    torch.cuda.synchronize()
+    st = layer.moe.device_status(layer.ws)
+    if st != 0:
+        raise SystemExit(f"{wl.name}: device status {st} ({layer.moe.status_string(st)})")
+    n_active = layer.active_experts()
+    parity = parity_check(layer, parity_tokens) if rank == 0 else {"ok": True, "checked_on": "rank 0"}
+    if not all_ranks_ok(parity["ok"], world, device):
+        return None, parity
+
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    step_ms, graph = time_steps(layer, steps, max(args.warmup, 3), not args.no_graph)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(statistics.mean(step_ms), world, device)
+    stats = step_stats(step_ms)
+    if steps < 50:
+        # Distribution over at least 50 steps (reported beside the K-step mean).
+        stats["over_50_steps"] = step_stats(time_steps(layer, 50, 3, not args.no_graph)[0])
+
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    stage = layer.dominant_stage()
+    st_ms = time_stage(layer, stage, reps=20)
+    e2e_ms = time_e2e(layer, max(20, min(steps, 200)), 3, graph)
+    breakdown = stage_breakdown(layer)
+    nograph_ms = statistics.mean(time_steps(layer, 50 if wl.T <= 64 else 10, 3, False)[0]) if not args.no_graph else ms
+    if layer.decode_path:
+        gu_bytes = layer.algorithmic_bytes_gateup(n_active)
+        achieved = gu_bytes / (st_ms / 1000.0) / 1e9
+        traffic, sha = traffic_from_profiles("dec_gateup", wl.name)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "kernel": "k_dec_gateup (MXFP4 gate/up GEMV + SwiGLU)",
+                "bytes_per_launch": gu_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
+    else:
+        fl = layer.flops_gateup()
+        achieved = fl / (st_ms / 1000.0) / 1e12
+        traffic, sha = traffic_from_profiles("pf_gateup", wl.name)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
+                "traffic": traffic, "kernel": "k_pf_gemm<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
+                "flops_per_launch": fl, "launch_ms": st_ms,
+                "hbm_frac_of_step": layer.algorithmic_bytes_step(n_active) / (ms / 1000.0) / 1e9 / hbm,
+                "peak_source": f"{peak_src} (bf16_tflops, burst; f16 operands run at the bf16 rate)"}
+    step_bytes = layer.algorithmic_bytes_step(n_active)
+    step_flops = layer.flops_step()
+    fields = {
+        "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s", "ms_per_step": ms,
+        "step_ms_stats": stats,
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "x_dtype": wl.x_dtype, "path": "decode" if layer.decode_path else "prefill",
+                   "path_arg": args.path, "cuda_graph": not args.no_graph,
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read; outside the step timing)",
+                   "active_experts": n_active, "parallelism": f"replicas x{world}"},
+        "weight_gbps": step_bytes / (ms / 1000.0) / 1e9,
+        "step_roofline": {"bytes": step_bytes, "frac_hbm": step_bytes / (ms / 1000.0) / 1e9 / hbm,
+                          "flops": step_flops, "tflops": step_flops / (ms / 1000.0) / 1e12,
+                          "frac_bf16": step_flops / (ms / 1000.0) / 1e12 / bf16},
+        "no_graph_ms_per_step": nograph_ms,
+        "stage_ms": breakdown,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": {"value": job_tokens_per_s(world, wl.T, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": layer.x.numel() * layer.x.element_size(),
+                "d2h_bytes_per_step": layer.out.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": layer.launches_per_step() * steps,
+        "wall_s_timed_region": t_wall,
+        "parity": parity,
+    }
+    if rank == 0:
+        fields["cpu_baseline"] = cpu_baseline(layer, cpu_seconds)
+    return fields, parity
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -567,82 +767,35 @@ def main():
     else:
         torch.cuda.set_device(0)
     device = f"cuda:{torch.cuda.current_device()}"
-    layer = Layer(args.workload, device)
+    layer = Layer(args.workload, device, path=PATHS[args.path])
     wl = layer.wl
-
-    # Untimed correctness probe through the library's device status word.
-    layer.step()
-    torch.cuda.synchronize()
-    st = layer.moe.device_status(layer.ws)
-    if st != 0:
-        raise SystemExit(f"device status {st} ({layer.moe.status_string(st)})")
-    n_active = layer.active_experts()
-
-    clocks = ClockSampler(local)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    t_wall = time.perf_counter()
-    step_ms, graph = time_steps(layer, args.steps, max(args.warmup, 3), not args.no_graph)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = max_over_ranks(statistics.mean(step_ms), world, device)
-    value = job_tokens_per_s(world, wl.T, ms)
-
-    hbm, bf16, bf16_sus, peak_src = peaks()
-    stage = layer.dominant_stage()
-    st_ms = time_stage(layer, stage, reps=20)
-    e2e_ms = time_e2e(layer, max(20, min(args.steps, 200)), 3, graph)
-    breakdown = stage_breakdown(layer)
-    nograph_ms = statistics.mean(time_steps(layer, 50, 3, False)[0]) if not args.no_graph else ms
-    if layer.decode_path:
-        gu_bytes = layer.algorithmic_bytes_gateup(n_active)
-        achieved = gu_bytes / (st_ms / 1000.0) / 1e9
-        traffic, sha = traffic_from_profiles("dec_gateup", wl.name)
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": traffic, "kernel": "k_dec_gateup (MXFP4 gate/up GEMV + SwiGLU)",
-                "bytes_per_launch": gu_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
-    else:
-        fl = layer.flops_gateup()
-        achieved = fl / (st_ms / 1000.0) / 1e12
-        traffic, sha = traffic_from_profiles("pf_gateup", wl.name)
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
-                "traffic": traffic, "kernel": "k_pf_gemm<gate/up> (tcgen05 kind::f16 grouped GEMM + SwiGLU)",
-                "flops_per_launch": fl, "launch_ms": st_ms,
-                "hbm_frac_of_step": layer.algorithmic_bytes_step(n_active) / (ms / 1000.0) / 1e9 / hbm,
-                "peak_source": f"{peak_src} (bf16_tflops, burst; f16 operands run at the bf16 rate)"}
-    step_bytes = layer.algorithmic_bytes_step(n_active)
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32" if wl.x_dtype == "f32" else "bf16 activations, MXFP4 weights, fp32 accumulate",
-        "data": "synthetic (seeded; 896 experts resident in HBM)",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
-                   "path": "decode" if layer.decode_path else "prefill", "cuda_graph": not args.no_graph,
-                   "l2": "flushed before every step (256 MiB write, then 256 MiB read; outside the step timing)",
-                   "active_experts": n_active, "parallelism": f"replicas x{world}"},
-        "weight_gbps": step_bytes / (ms / 1000.0) / 1e9,
-        "step_roofline": {"bytes": step_bytes, "frac_hbm": step_bytes / (ms / 1000.0) / 1e9 / hbm,
-                          "tflops": layer.flops_step() / (ms / 1000.0) / 1e12},
-        "no_graph_ms_per_step": nograph_ms,
-        "stage_ms": breakdown,
-        "roofline": roof,
-        "clocks": clk,
-        "e2e": {"value": job_tokens_per_s(world, wl.T, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": layer.x.numel() * layer.x.element_size(),
-                "d2h_bytes_per_step": layer.out.numel() * 4, "ms_per_step": e2e_ms},
-        "gpu_launches": layer.launches_per_step() * args.steps,
-        "wall_s_timed_region": t_wall,
-    }
+    fields, parity = measure(layer, args, rank, world, local, device, args.steps, args.cpu_seconds, 3)
+    base = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ("f32 activations" if wl.x_dtype == "f32" else "bf16 activations") +
+                     ", MXFP4 weights, fp32 accumulate",
+            "data": "synthetic (seeded; 896 experts resident in HBM)"}
+    if fields is None:
+        if rank == 0:
+            print(json.dumps(dict(base, value=None, unit="tokens/s", parity=parity,
+                                  error="parity against the oracle failed: nothing timed")), flush=True)
+        raise SystemExit(1)
+    line = dict(base, **fields)
+    if args.workload == "decode" and args.path == "auto" and not args.no_prefill_leg:
+        # The 4096-token Zipf prefill on the same resident experts (they
+        # depend on H, E, I and the seed only).
+        long_layer = Layer("long", device, table=layer.table)
+        lf, lparity = measure(long_layer, args, rank, world, local, device, args.steps,
+                              min(args.cpu_seconds, 5.0), 2)
+        if lf is None:
+            if rank == 0:
+                line["prefill_long"] = {"value": None, "parity": lparity,
+                                        "error": "parity against the oracle failed: nothing timed"}
+                print(json.dumps(line), flush=True)
+            raise SystemExit(1)
+        line["prefill_long"] = lf
+        del long_layer
     if rank == 0:
-        cb, parity = cpu_baseline(layer, args.cpu_seconds)
-        line["cpu_baseline"] = cb
-        line["parity_on_cpu_sample"] = parity
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()

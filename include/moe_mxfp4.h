@@ -62,9 +62,9 @@
  *   - Errors: argument problems are reported before anything is launched
  *     (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE); a launch
  *     failure returns MOE_ERR_CUDA.  Problems the kernels detect (an expert id
- *     out of range, a bounded wait that gave up, a range overflow in the fp16
- *     operands of the prefill path) set a status word inside `ws` that
- *     moe_device_status() reads; outputs of such a call are unspecified.
+ *     or bucket entry out of range, a bounded wait that gave up) set a status
+ *     word inside `ws` that moe_device_status() reads; outputs of such a call
+ *     are unspecified.
  *   - Workspace: `ws` must hold moe_workspace_bytes(shape) bytes; its contents
  *     need not be initialised and are overwritten.  One workspace must not be
  *     used by two calls that may run concurrently.
@@ -95,7 +95,7 @@ typedef enum {
   MOE_ERR_CUDA = 4,         /* a CUDA launch or query failed */
   MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
   MOE_ERR_DEVICE_CHECK = 6, /* device: an expert id out of [0, E) */
-  MOE_ERR_RANGE = 7         /* device: a prefill fp16 operand overflowed */
+  MOE_ERR_RANGE = 7         /* reserved: no call of this version raises it */
 } moe_status;
 
 /* Activation element types. */
@@ -116,8 +116,10 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
  *   auto:    decode for T <= MOE_DECODE_MAX_T or fp32 x; else decode while
  *            the batch has at most MOE_DECODE_AUTO_PAIRS_PER_EXPERT routed
  *            pairs per expert (T * k <= that * E) and T <=
- *            MOE_DECODE_BATCH_MAX_T; else prefill.  The bound is the measured crossover of the two paths
- *            on GB300: below it the decode path's single pass over the
+ *            MOE_DECODE_BATCH_MAX_T; else prefill.  A bf16 shape that the
+ *            decode kernels do not take (H > 8192) goes to prefill when that
+ *            path takes it.  The bound is the measured crossover of the two
+ *            paths on GB300: below it the decode path's single pass over the
  *            active experts' weights is faster than the tensor-core GEMMs,
  *            whose per-tile cost needs many tokens per expert. */
 typedef enum {
@@ -214,7 +216,10 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
  *   - Set-up: the first call on a device (that device current) looks up the
  *     scratch address once; a CUDA failure there returns MOE_ERR_CUDA.  If the
  *     caller records its work into a CUDA graph, make one call before
- *     recording so that this set-up is not part of the recorded work.
+ *     recording so that this set-up is not part of the recorded work.  The
+ *     address is kept for the life of the process: after cudaDeviceReset()
+ *     on a device (or in another driver context on it) the kept address is
+ *     stale, and this entry point must not be called there again.
  *   - Contents: the scratch needs no initialisation; every call resets what it
  *     relies on (the status word and the counters) at its start.
  *   - Concurrency: all calls on one device share the one scratch region.  Two

@@ -55,6 +55,11 @@ int resolve_path(const moe_shape* s, int x_dtype, bool has_shared, int path, int
       path = MOE_PATH_DECODE;
     else
       path = MOE_PATH_PREFILL;
+    // A shape the decode kernels do not take (e.g. H > 8192) runs on the
+    // prefill path when that path takes it.
+    if (path == MOE_PATH_DECODE && !decode_experts_supported(s, x_dtype) && x_dtype == MOE_DT_BF16 &&
+        prefill_supported(s->H, s->I))
+      path = MOE_PATH_PREFILL;
   }
   if (path == MOE_PATH_DECODE) {
     if (!decode_experts_supported(s, x_dtype)) return MOE_ERR_UNSUPPORTED;
@@ -209,7 +214,7 @@ const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "a CUDA launch or query failed";
     case MOE_ERR_TIMEOUT: return "a bounded device wait gave up";
     case MOE_ERR_DEVICE_CHECK: return "device check failed: expert id or bucket entry out of range";
-    case MOE_ERR_RANGE: return "prefill fp16 operand out of range";
+    case MOE_ERR_RANGE: return "reserved status (not raised by this version)";
     default: return "unknown status";
   }
 }
@@ -298,6 +303,7 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
     if ((st = cuda_status(cudaMemsetAsync(&L.hdr->n_active, 0, sizeof(uint32_t), s))) != MOE_OK) return st;
     ExpertParams ps = p;
     ps.accumulate = 1;
+    ps.shared_only = 1;
     return cuda_status(launch_prefill_experts(ps, s));
   }
   if ((st = do_route(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L, false, s)) != MOE_OK) return st;

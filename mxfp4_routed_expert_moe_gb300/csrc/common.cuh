@@ -45,8 +45,11 @@ struct Ws {
   int32_t* act_pref_dn; // [E+1]   prefix of prefill down tiles per active expert
   uint16_t* xh;         // [T][H]  fp16 activations (prefill)
   float* xscale;        // [T]     2^-sigma_t of the fp16 activations
-  void* h;              // [T*k][I] fp32 (decode) or [T*k + T][I] fp16 (prefill; rows
+  void* h;              // fp32 h: [T*k][I] (decode) or [T*k + T][I] (prefill; rows
                         // T*k.. hold the shared expert's h)
+  uint16_t* h16;        // [T*k + T][I] prefill: f16 h scaled by 2^tau_row (aliases y)
+  uint32_t* hmax;       // [T*k + T]  prefill: bits of max |h| over each h row
+  float* hscale;        // [T*k + T]  prefill: 2^-tau_row of each f16 h row
   int32_t* shsig;       // [2I + H] row shifts of the bf16 shared expert (gate, up, down)
   float* y;             // [T*k][H] fp32 (decode, T <= 1024)
   float2* rpart;        // [S][T][E] router partial sums of the S K-splits (S > 1 only)
@@ -98,11 +101,20 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.xscale = (float*)take(T * 4);
   // Tokens the decode path may take for this shape (0: it cannot).
   const size_t Td = T <= (size_t)kDecodeBatchMaxT ? T : 0;
-  // h: fp32 for the decode path (Td*k rows), fp16 for the prefill path (T*k rows).
-  const size_t h_dec = Td * k * I * 4, h_pf = (T * k + T) * I * 2;
+  // h in fp32: Td*k rows for the decode path, T*k + T rows for the prefill
+  // path (routed pairs, then the shared expert's tokens).
+  const size_t hrows = T * k + T;
+  const size_t h_dec = Td * k * I * 4, h_pf = hrows * I * 4;
   ws.h = (void*)take(h_dec > h_pf ? h_dec : h_pf);
+  ws.hmax = (uint32_t*)take(hrows * 4);
+  ws.hscale = (float*)take(hrows * 4);
   ws.shsig = (int32_t*)take((2 * I + H) * 4);
-  ws.y = (float*)take(Td * k * H * 4);
+  // y (decode) and the prefill path's f16 h share one region: the prefill
+  // kernels run on the decode path only for the shared expert, after the
+  // routed experts' combine has consumed y.
+  const size_t y_dec = Td * k * H * 4, h16_pf = hrows * I * 2;
+  ws.y = (float*)take(y_dec > h16_pf ? y_dec : h16_pf);
+  ws.h16 = (uint16_t*)ws.y;
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
   const size_t S = (size_t)router_splits(s.T, s.E, s.H);
   ws.rpart = (float2*)take(S > 1 ? S * T * E * 8 : 0);
@@ -327,6 +339,7 @@ struct ExpertParams {
   int accumulate;
   const moe_dense_bf16* shared_dev;  // unused on device; shared pointers below
   const uint16_t *sh_gate, *sh_up, *sh_down;
+  int shared_only;       // prefill kernels: the shared expert alone (decode path), no routed h rows
   int fused_route;       // decode: the gate/up kernel routes (from ws.logits) first
   RouteParams rp;        // the route to compute when fused_route
   Ws ws;

@@ -15,8 +15,13 @@
 //     [2^14, 2^15)), exact for bf16 inputs.
 //   * Products are exact and accumulate in fp32 in Tensor Memory; the
 //     epilogue removes both shifts.
-// gate/up: the epilogue applies SwiGLU and stores h in f16, bucket order.
-// down: the epilogue adds w[t][j] * y into out with fp32 atomics.
+// gate/up: the epilogue applies SwiGLU and stores h in fp32, bucket order,
+// raising the largest |h| of each h row; a pass then writes each row in f16
+// scaled by a power of two that puts its largest magnitude in [2^14, 2^15)
+// (no overflow for any finite h; 11 significant bits for every element within
+// 2^28 of the row's maximum).
+// down: the epilogue removes that shift and adds w[t][j] * y into out with
+// fp32 atomics.
 // The optional bf16 shared expert runs as extra work items of the same
 // kernels (identity token map, weight 1); its rows get the same kind of
 // power-of-two shift, computed by a pre-pass.
@@ -72,10 +77,41 @@ static_assert(kPfEpWarps == 4 && (kPfDqWarps + kPfLdWarps) % 4 == 0, "epilogue w
 
 // ------------------------------------------------------------ pre-passes --
 // xh[t][h] = f16(x[t][h] * 2^sigma_t), xscale[t] = 2^-sigma_t (one CTA per token).
+// Also clears the h-row maxima of token t's routed pairs and of its
+// shared-expert row, which the gate/up epilogue raises with atomicMax.
 __global__ void __launch_bounds__(256) k_x_to_f16(ExpertParams p) {
   const int t = blockIdx.x;
   x_row_to_f16(reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * p.H, p.H, p.ws.xh + (size_t)t * p.H,
                &p.ws.xscale[t]);
+  if ((int)threadIdx.x < p.k) p.ws.hmax[(size_t)t * p.k + threadIdx.x] = 0u;
+  if (threadIdx.x == 0) p.ws.hmax[(size_t)p.T * p.k + t] = 0u;
+}
+
+// f16 copy of the fp32 h rows [row0, row1) for the down GEMM: row r is scaled
+// by 2^tau_r, tau_r = 14 - floor(log2 max|h_r|), which puts the row's largest
+// magnitude in [2^14, 2^15): no overflow, and every element within 2^28 of the
+// maximum keeps the full 11-bit f16 significand.  hscale[r] = 2^-tau_r is
+// removed in the down epilogue.  A row whose maximum is zero, infinite or NaN
+// keeps tau = 0 (NaN and infinity propagate).  One warp per row; I % 32 == 0.
+__global__ void __launch_bounds__(256) k_h_to_f16(ExpertParams p, int row0, int row1) {
+  const int row = row0 + blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= row1) return;
+  const uint32_t m = p.ws.hmax[row];
+  const int e = (int)((m >> 23) & 0xFFu);
+  int tau = (m == 0u || e == 0xFF) ? 0 : 14 - (e - 127);
+  tau = tau > 100 ? 100 : (tau < -100 ? -100 : tau);
+  const float up = __int_as_float((tau + 127) << 23);
+  if (lane == 0) p.ws.hscale[row] = __int_as_float((127 - tau) << 23);
+  const float* src = reinterpret_cast<const float*>(p.ws.h) + (size_t)row * p.I;
+  uint16_t* dst = p.ws.h16 + (size_t)row * p.I;
+  for (int c = lane * 4; c < p.I; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(src + c);
+    const __half2 a = __floats2half2_rn(v.x * up, v.y * up);
+    const __half2 b = __floats2half2_rn(v.z * up, v.w * up);
+    *reinterpret_cast<uint2*>(dst + c) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
 }
 
 cudaError_t launch_x_to_f16(const ExpertParams& p, cudaStream_t s) {
@@ -503,7 +539,7 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
       src[j] = nullptr;
       if (n < it.cnt) {
         if (!GATEUP) {
-          src[j] = reinterpret_cast<const uint16_t*>(p.ws.h) + (size_t)(it.hpos0 + n) * p.I + ch * 8;
+          src[j] = p.ws.h16 + (size_t)(it.hpos0 + n) * p.I + ch * 8;
         } else if (it.shared) {
           src[j] = p.ws.xh + (size_t)(it.p0 + n) * p.H + ch * 8;
         } else {
@@ -618,7 +654,7 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
         wgt = __ldg(&p.w[pr]);
       }
       col_tok[n] = t;
-      col_scale[n] = GATEUP ? __ldg(&p.ws.xscale[t]) : wgt;
+      col_scale[n] = GATEUP ? __ldg(&p.ws.xscale[t]) : wgt * __ldg(&p.ws.hscale[it.hpos0 + n]);
     }
     __syncwarp();
     if (!pf_warp_wait(c, &sh.accf[b], (ci >> 1) & 1)) break;
@@ -631,21 +667,27 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
         uint32_t u[16];
         tmem_ld16(tbase + 128u + (uint32_t)c0, u);
         tmem_ld_wait();
-        if (valid) {
-          __half* hout = reinterpret_cast<__half*>(p.ws.h);
+        // h in fp32, and the largest |h| of each column (h row) over this
+        // warp's 32 weight rows raised into hmax (non-negative floats order
+        // as their bits; NaN orders above infinity).
+        float* hout = reinterpret_cast<float*>(p.ws.h);
+        uint32_t habs = 0u;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = c0 + i;
-            if (n < it.cnt) {
-              const float xs = col_scale[n];
-              const float gv = __uint_as_float(g[i]) * rs0 * xs;
-              const float uv = __uint_as_float(u[i]) * rs1 * xs;
-              const float hv = silu_f32(gv) * uv;
-              if (fabsf(hv) > 65504.f) set_status(c.hdr, MOE_ERR_RANGE);
-              hout[(size_t)(it.hpos0 + n) * p.I + row] = __float2half_rn(hv);
-            }
+        for (int i = 0; i < 16; ++i) {
+          const int n = c0 + i;
+          uint32_t a = 0u;
+          if (valid && n < it.cnt) {
+            const float xs = col_scale[n];
+            const float gv = __uint_as_float(g[i]) * rs0 * xs;
+            const float uv = __uint_as_float(u[i]) * rs1 * xs;
+            const float hv = silu_f32(gv) * uv;
+            hout[(size_t)(it.hpos0 + n) * p.I + row] = hv;
+            a = __float_as_uint(hv) & 0x7FFFFFFFu;
           }
+          const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, a);
+          if (lane == i) habs = mx;
         }
+        if (lane < 16 && c0 + lane < it.cnt && habs != 0u) atomicMax(&p.ws.hmax[it.hpos0 + c0 + lane], habs);
       } else {
         tmem_ld_wait();
         if (valid) {
@@ -827,6 +869,14 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(p);
   prof_after(MOE_STAGE_PF_GATEUP, s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  // f16 h rows for the down GEMM: the routed pairs' rows (none when the
+  // shared expert runs alone) and the shared expert's.
+  const int hrow0 = p.shared_only ? p.T * p.k : 0;
+  const int hrow1 = p.T * p.k + (p.sh_gate ? p.T : 0);
+  if (hrow1 > hrow0) {
+    k_h_to_f16<<<(hrow1 - hrow0 + 7) / 8, 256, 0, s>>>(p, hrow0, hrow1);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   prof_before(MOE_STAGE_PF_DOWN, s);
   k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(p);
   prof_after(MOE_STAGE_PF_DOWN, s);

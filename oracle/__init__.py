@@ -57,7 +57,6 @@ def lib():
             L.orc_dequant.argtypes = [vp, vp, i64, i64, vp]
             L.orc_router_logits.argtypes = [i32, i32, i32, vp, i32, vp, vp, i32, vp]
             L.orc_topk.argtypes = [i32, i32, i32, vp, vp, vp, vp]
-            L.orc_router_bound.argtypes = [i32, i32, i32, vp, i32, vp, vp, vp]
             L.orc_bucket.argtypes = [i32, i32, i32, vp, vp, vp]
             L.orc_expert_mlp.argtypes = [i32, i32, vp, ctypes.POINTER(_Expert), vp]
             L.orc_dense_mlp_bf16.argtypes = [i32, i32, vp, vp, vp, vp, vp]
@@ -125,18 +124,6 @@ def topk(s, k):
     margin = np.empty(T, dtype=np.float64)
     _check(lib().orc_topk(T, E, k, s.ctypes.data, ids.ctypes.data, w.ctypes.data, margin.ctypes.data), "orc_topk")
     return ids, w, margin
-
-
-def router_bound(x, wr, br=None):
-    x = np.ascontiguousarray(x)
-    wr = np.ascontiguousarray(wr, dtype=np.float32)
-    T, H = x.shape
-    E = wr.shape[0]
-    br = None if br is None else np.ascontiguousarray(br, dtype=np.float32)
-    b = np.empty((T, E), dtype=np.float64)
-    _check(lib().orc_router_bound(T, H, E, x.ctypes.data, _dtype_code(x), wr.ctypes.data, _ptr(br),
-                                  b.ctypes.data), "orc_router_bound")
-    return b
 
 
 def bucket(ids, E):

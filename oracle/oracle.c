@@ -229,26 +229,6 @@ int orc_topk(int T, int E, int k, const double* s, int32_t* ids, double* w, doub
   return ORC_OK;
 }
 
-/* Per-score error bound of an fp32 evaluation of s[t][e] in any summation
- * order: gamma_{H+1} * (sum_h |x[t][h] Wr[e][h]| + |b[e]|), with
- * gamma_n = n u / (1 - n u), u = 2^-24.  Written to bound [T][E]. */
-int orc_router_bound(int T, int H, int E, const void* x, int dtype, const float* wr, const float* br,
-                     double* bound) {
-  if (T < 0 || H < 1 || E < 1) return ORC_EINVAL;
-  const double u = ldexp(1.0, -24);
-  const double n = (double)(H + 1);
-  const double gamma = n * u / (1.0 - n * u);
-  for (int t = 0; t < T; ++t)
-    for (int e = 0; e < E; ++e) {
-      double a = 0.0;
-      for (int h = 0; h < H; ++h)
-        a += fabs(orc_act(x, dtype, (int64_t)t * H + h) * (double)wr[(int64_t)e * H + h]);
-      if (br) a += fabs((double)br[e]);
-      bound[(int64_t)t * E + e] = gamma * a;
-    }
-  return ORC_OK;
-}
-
 /* ------------------------------------------------------------- bucketing -- */
 
 /* Counting sort of the flat pairs i = t*k + j by expert ids[t][j]:

@@ -198,6 +198,8 @@ WORKLOADS = {
     "prefill": Workload("prefill_T512_H7168_E896_k16_I1408_shared", 512, 7168, 896, 16, 1408, shared=True),
     "long": Workload("long_prefill_T4096_H7168_E896_k16_I1408_zipf1.1", 4096, 7168, 896, 16, 1408, routing="zipf"),
     "decode_i1536": Workload("decode_T1_H7168_E896_k16_I1536", 1, 7168, 896, 16, 1536),
+    # 1-token decode with fp32 activations (the pages keep activations in fp32).
+    "decode_f32": Workload("decode_f32_T1_H7168_E896_k16_I1408", 1, 7168, 896, 16, 1408, x_dtype="f32"),
     # A 256-token batch of the full layer: the decode path's batched kernels.
     "batch256": Workload("batch_decode_T256_H7168_E896_k16_I1408", 256, 7168, 896, 16, 1408),
     # Small-footprint case of the decode kernels for profiler captures: 32

@@ -150,6 +150,16 @@ def test_select_path_rules(moe):
     with pytest.raises(moe.MoeError) as ei:
         sel(1, 7168 + 32, E, I, k, shared=True)
     assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    # A bf16 shape the decode kernels do not take (H > 8192) goes to the
+    # prefill path when that path takes it (H, I % 128 == 0); fp32 cannot.
+    assert sel(1, 12288, E, I, k) == P
+    assert sel(64, 16384, E, I, k) == P
+    with pytest.raises(moe.MoeError) as ei:
+        sel(1, 12288, E, I, k, path=D)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as ei:
+        sel(1, 12288, E, I, k, x_dtype=moe.DT_F32)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
     # Explicit paths.
     assert sel(512, H, 64, I, k, path=D) == D
     assert sel(1, H, E, I, k, path=P) == P

@@ -113,15 +113,6 @@ def test_margin_is_smallest_adjacent_gap():
     assert margin[0] == 0.5
 
 
-def test_router_bound_formula():
-    x, wr = _rand_router(2, 64, 3, 6)
-    b = oracle.router_bound(x, wr)
-    u = 2.0 ** -24
-    g = 65 * u / (1 - 65 * u)
-    ref = g * np.abs(x.astype(np.float64)[:, None, :] * wr.astype(np.float64)[None, :, :]).sum(-1)
-    np.testing.assert_allclose(b, ref, rtol=1e-12)
-
-
 def _bucket_brute(ids, E):
     T, k = ids.shape
     pairs = sorted((int(ids[t, j]), t, j) for t in range(T) for j in range(k))

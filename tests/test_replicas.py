@@ -25,7 +25,9 @@ def _rank_main(rank, world, port, q):
     try:
         r, w, local = bench.dist_env()
         ms = bench.max_over_ranks(2.0 + rank, w, "cpu")  # rank 1 is the slower one
-        q.put((r, w, local, ms, bench.job_tokens_per_s(w, 512, ms)))
+        # A parity failure on one rank stops every rank before the timing.
+        agree = (bench.all_ranks_ok(True, w, "cpu"), bench.all_ranks_ok(rank == 0, w, "cpu"))
+        q.put((r, w, local, ms, bench.job_tokens_per_s(w, 512, ms), agree))
     finally:
         dist.destroy_process_group()
 
@@ -42,8 +44,9 @@ def test_two_replicas_report_slowest_time_and_summed_throughput():
         p.join(timeout=120)
         assert p.exitcode == 0
     res = sorted(q.get(timeout=10) for _ in range(2))
-    for rank, (r, w, local, ms, tps) in enumerate(res):
+    for rank, (r, w, local, ms, tps, agree) in enumerate(res):
         assert (r, w, local) == (rank, 2, rank)
+        assert agree == (True, False)
         assert ms == pytest.approx(3.0)
         assert tps == pytest.approx(2 * 512 / 3.0e-3)
 
@@ -54,3 +57,11 @@ def test_single_process_defaults():
         os.environ.pop(k, None)
     assert bench.dist_env() == (0, 1, 0)
     assert bench.max_over_ranks(1.5, 1, "cpu") == 1.5
+
+
+def test_step_stats():
+    import bench
+    st = bench.step_stats([float(v) for v in range(1, 101)])
+    assert st["n"] == 100 and st["min"] == 1.0 and st["max"] == 100.0
+    assert st["median"] == 50.5 and st["mean"] == 50.5
+    assert st["p10"] == 11.0 and st["p90"] == 90.0

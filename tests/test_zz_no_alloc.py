@@ -37,9 +37,14 @@ def _compare(name, wl, path):
         assert int(status.item()) == 0, f"{name} call {call}: device status {int(status.item())}"
         assert t.equal(ids, ids_ref), f"{name} call {call}: ids differ"
         assert float((w - w_ref).abs().max()) <= 1e-6
-        a, b = out.cpu().numpy().astype(np.float64), ref.cpu().numpy().astype(np.float64)
-        rel = np.linalg.norm(a - b) / np.linalg.norm(b)
-        assert rel <= 1e-5, f"{name} call {call}: rel-L2 {rel:.2e} against moe_forward"
+        if path == 1:
+            # The decode path sums in a fixed order: bitwise the same result.
+            assert t.equal(out, ref), f"{name} call {call}: output differs from moe_forward"
+        else:
+            # The prefill path combines with fp32 atomics (order not fixed).
+            a, b = out.cpu().numpy().astype(np.float64), ref.cpu().numpy().astype(np.float64)
+            rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+            assert rel <= 1e-5, f"{name} call {call}: rel-L2 {rel:.2e} against moe_forward"
 
 
 @pytest.mark.gpu
