@@ -216,15 +216,16 @@ class Layer:
 
     def launches_per_step(self) -> int:
         # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
-        # shifts), gate/up, down
+        # shifts), item tables, gate/up, h->fp16, down
         if self.decode_path:
-            # shared expert: x->fp16, its row shifts, and the two prefill GEMMs on its tiles alone
-            sh = 4 if self.shared is not None else 0
+            # shared expert: x->fp16, its row shifts, item tables, and the two prefill GEMMs (with
+            # the h->fp16 pass between them) on its tiles alone
+            sh = 6 if self.shared is not None else 0
             if self.wl.T <= self.moe.DECODE_MAX_T:
                 return 3 + sh  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
             # router GEMM (+ split reduction), top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
             return 8 + sh + (1 if self._router_splits() > 1 else 0)
-        return 7 + (1 if self.shared is not None else 0) + (1 if self._router_splits() > 1 else 0)
+        return 9 + (1 if self.shared is not None else 0) + (1 if self._router_splits() > 1 else 0)
 
     def _router_splits(self) -> int:
         """Splits of the router GEMM's contraction (the library's rule)."""

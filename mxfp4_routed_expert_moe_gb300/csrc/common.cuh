@@ -43,6 +43,8 @@ struct Ws {
   int32_t* act_e;       // [E]     active experts, ascending
   int32_t* act_pref_gu; // [E+1]   prefix of prefill gate/up tiles per active expert
   int32_t* act_pref_dn; // [E+1]   prefix of prefill down tiles per active expert
+  int4* items_gu;       // prefill gate/up work items {e (-1: shared expert), m0, p0, cnt}
+  int4* items_dn;       // prefill down work items, the same fields
   uint16_t* xh;         // [T][H]  fp16 activations (prefill)
   float* xscale;        // [T]     2^-sigma_t of the fp16 activations
   void* h;              // fp32 h: [T*k][I] (decode) or [T*k + T][I] (prefill; rows
@@ -97,6 +99,17 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.act_e = (int32_t*)take(E * 4);
   ws.act_pref_gu = (int32_t*)take((E + 1) * 4);
   ws.act_pref_dn = (int32_t*)take((E + 1) * 4);
+  {
+    // Work items of the prefill GEMMs: (active expert, 128-row tile, token
+    // tile of up to 128), then the shared expert's tiles.  The token tiles of
+    // all active experts number at most ceil(T*k/128) + min(E, T*k).
+    const size_t pairs = T * k;
+    const size_t ntiles = (pairs + 127) / 128 + (E < pairs ? E : pairs);
+    const size_t shtiles = (T + 127) / 128;
+    const size_t mgu = (I + 127) / 128, mdn = (H + 127) / 128;
+    ws.items_gu = (int4*)take((ntiles + shtiles) * mgu * 16);
+    ws.items_dn = (int4*)take((ntiles + shtiles) * mdn * 16);
+  }
   ws.xh = (uint16_t*)take(T * H * 2);
   ws.xscale = (float*)take(T * 4);
   // Tokens the decode path may take for this shape (0: it cannot).

@@ -39,41 +39,55 @@
 namespace moe {
 
 constexpr int kPfSliceK = 64;            // contraction elements per stage (one 128-byte swizzle row)
-constexpr int kPfTileBytes = 128 * 128;  // one 128-row x 64-element f16 tile
-// Weight dequant: two groups of 8 warps; group k converts the slices of parity
-// k (2 threads per weight row in each group), so each warp's per-slice chain
-// of waits, conversion and signalling overlaps the other group's.
-constexpr int kPfDqGroups = 2;
-constexpr int kPfDqGroupWarps = 8;
-constexpr int kPfDqGroupThreads = kPfDqGroupWarps * 32;
-constexpr int kPfDqWarps = kPfDqGroups * kPfDqGroupWarps;  // warps 0-15
-constexpr int kPfLdWarps = 4;            // warps 16-19: token rows (cp.async)
-constexpr int kPfEpWarps = 4;            // warps 20-23: epilogue (warp % 4 = TMEM lane quarter)
+constexpr int kPfTileBytes = 128 * 128;  // one 128-row x 64-element f16 token tile
+// Roles: 16 dequant warps (one weight row per thread and matrix; they write
+// the f16 A operand straight into Tensor Memory), 4 loader warps (token rows,
+// cp.async), 4 epilogue warps (warp % 4 = TMEM lane quarter), 2 MMA issuers.
 // MMA issue: one thread issues a tcgen05.mma only every ~100 cycles whatever
 // its size, so the gate/up kernel issues from two warps, one accumulator each
-// (gate, up).  The down kernel has one accumulator and one issuer.
-constexpr int kPfMmaWarp = kPfDqWarps + kPfLdWarps + kPfEpWarps;  // warps 24-25: MMA issuers; 24 owns TMEM
+// (gate, up).  The down kernel has one accumulator per buffer and one issuer.
+constexpr int kPfDqWarps = 16;           // warps 0-15
+constexpr int kPfLdWarps = 4;            // warps 16-19
+constexpr int kPfEpWarps = 4;            // warps 20-23
+constexpr int kPfMmaWarp = kPfDqWarps + kPfLdWarps + kPfEpWarps;  // warps 24-25; 24 owns TMEM
 constexpr int kPfMmaWarps = 2;
 constexpr int kPfThreads = (kPfMmaWarp + kPfMmaWarps) * 32;
 constexpr int kPfMaxStages = 8;
-// Rings (per kernel): f16 weight tiles from the dequant warps (A), f16 token
-// rows from the loader warps (B), raw MXFP4 bytes of the dequant threads.
-constexpr int kPfAStagesGateUp = 3, kPfBStagesGateUp = 5;
-constexpr int kPfAStagesDown = 3, kPfBStagesDown = 6;
 constexpr int kPfL2Window = 256;         // bytes of each weight row prefetched into L2 at a time
-constexpr uint32_t kPfTmemCols = 512;    // 2 accumulator buffers x (gate 128 + up 128) columns
+constexpr uint32_t kPfTmemCols = 512;
+constexpr uint32_t kPfAccCols = 256;     // TMEM columns [0, 256): accumulators; [256, 512): A stages
 constexpr int kPfSigRing = 4;            // items whose row shifts are published ahead
-// Raw MXFP4 ring of each dequant group: per slice and thread 16 bytes of
-// codes and the 4-byte scale word per matrix, cp.async'd this many of the
-// group's slices ahead (about 48 KB in flight per SM for either kernel).
-constexpr int kPfRawGateUp = 2;
-constexpr int kPfRawDown = 6;
-template <int NA>
-struct PfRaw {
-  static constexpr int kQ = NA * kPfDqGroupThreads * 16;              // codes
-  static constexpr int kStage = kQ + NA * kPfDqGroupThreads * 4;      // + scale words
+// Per kernel:
+//   NA    matrices per item (gate/up: 2, down: 1)
+//   GW    warps of one dequant group (4 per matrix: one TMEM lane quarter
+//         each); a group fills one A stage, and the NG groups take turns
+//         over the CTA's slices
+//   ACCB  accumulator buffers: gate/up one (gate columns 0-127, up 128-255),
+//         down two of 128 columns (the epilogue of one item overlaps the
+//         next item's MMAs)
+//   AS    A stages in TMEM, ACOLS columns each (64 f16 of a row = 32 columns
+//         per matrix)
+//   BS    token ring stages (shared memory)
+//   R     raw MXFP4 slots per dequant group (its slices copied ahead)
+template <bool GATEUP>
+struct PfCfg {
+  static constexpr int NA = GATEUP ? 2 : 1;
+  static constexpr int GW = 4 * NA;
+  static constexpr int NG = kPfDqWarps / GW;
+  static constexpr int ACCB = GATEUP ? 1 : 2;
+  static constexpr int ACCW = GATEUP ? 256 : 128;  // columns per accumulator buffer
+  static constexpr int ACOLS = 32 * NA;
+  static constexpr int AS = (int)(kPfTmemCols - kPfAccCols) / ACOLS;  // 4 or 8
+  static constexpr int BS = 6;
+  static constexpr int R = GATEUP ? 3 : 4;
+  // Raw slot: the 32 bytes of codes of each group thread (first 16 bytes of
+  // every thread, then the second 16), then its 4-byte scale word.
+  static constexpr int kThreads = GW * 32;
+  static constexpr int kQ = kThreads * 32;
+  static constexpr int kStage = kQ + kThreads * 4;
 };
 static_assert(kPfEpWarps == 4 && (kPfDqWarps + kPfLdWarps) % 4 == 0, "epilogue warps must cover lane quarters 0-3");
+static_assert(PfCfg<true>::AS <= kPfMaxStages && PfCfg<false>::AS <= kPfMaxStages, "A stages");
 
 // ------------------------------------------------------------ pre-passes --
 // xh[t][h] = f16(x[t][h] * 2^sigma_t), xscale[t] = 2^-sigma_t (one CTA per token).
@@ -164,38 +178,55 @@ struct PfItem {
   int hpos0;   // row of the tile's first token in h ([T*k + T][I])
 };
 
-__device__ __forceinline__ PfItem pf_item(int item, const ExpertParams& p, const int32_t* pref, int U,
-                                          int n_routed) {
-  PfItem it;
-  if (item >= n_routed) {
-    const int local = item - n_routed;
+// Item tables of both GEMMs, written once per call from the bucket layout
+// (so each role reads an item with one load): for every active expert u its
+// items [pref[u], pref[u+1]) in row-tile-major order, then the shared
+// expert's items.  One warp per active expert.
+__device__ __forceinline__ void pf_fill_items(const ExpertParams& p, const int32_t* pref, int4* items, int M, int u,
+                                              int U) {
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (M + kPfMTile - 1) / kPfMTile;
+  if (u < U) {
+    const int e = p.ws.act_e[u];
+    const int b0 = p.offsets[e];
+    const int n = p.offsets[e + 1] - b0;
+    const int ntiles = (n + kPfNTile - 1) / kPfNTile;
+    const int base = pref[u];
+    const int count = ntiles * m_tiles;
+    for (int local = lane; local < count; local += 32) {
+      const int m = local / ntiles, nt = local - m * ntiles;
+      items[base + local] = make_int4(e, m * kPfMTile, b0 + nt * kPfNTile, min(kPfNTile, n - nt * kPfNTile));
+    }
+  } else if (p.sh_gate) {
+    const int base = U > 0 ? pref[U] : 0;
     const int nts = (p.T + kPfNTile - 1) / kPfNTile;
-    const int m = local / nts, nt = local - m * nts;
-    it.shared = 1;
-    it.e = 0;
-    it.m0 = m * kPfMTile;
-    it.p0 = nt * kPfNTile;
-    it.cnt = min(kPfNTile, p.T - it.p0);
-    it.hpos0 = p.T * p.k + it.p0;
-    return it;
+    for (int local = lane; local < m_tiles * nts; local += 32) {
+      const int m = local / nts, nt = local - m * nts;
+      items[base + local] = make_int4(-1, m * kPfMTile, nt * kPfNTile, min(kPfNTile, p.T - nt * kPfNTile));
+    }
   }
-  int lo = 0, hi = U - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&pref[mid]) <= item) lo = mid; else hi = mid - 1;
+}
+
+__global__ void __launch_bounds__(256) k_pf_items(ExpertParams p) {
+  const int U = (int)p.ws.hdr->n_active;
+  const int nwarps = (int)(gridDim.x * blockDim.x) >> 5;
+  for (int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); w <= 2 * U + 1; w += nwarps) {
+    if (w <= U)
+      pf_fill_items(p, p.ws.act_pref_gu, p.ws.items_gu, p.I, w, U);
+    else
+      pf_fill_items(p, p.ws.act_pref_dn, p.ws.items_dn, p.H, w - U - 1, U);
   }
-  const int local = item - __ldg(&pref[lo]);
-  const int e = __ldg(&p.ws.act_e[lo]);
-  const int b0 = __ldg(&p.offsets[e]);
-  const int n = __ldg(&p.offsets[e + 1]) - b0;
-  const int ntiles = (n + kPfNTile - 1) / kPfNTile;
-  const int m = local / ntiles, nt = local - m * ntiles;
-  it.shared = 0;
-  it.e = e;
-  it.m0 = m * kPfMTile;
-  it.p0 = b0 + nt * kPfNTile;
-  it.cnt = min(kPfNTile, n - nt * kPfNTile);
-  it.hpos0 = it.p0;
+}
+
+__device__ __forceinline__ PfItem pf_item(int item, const ExpertParams& p, const int4* items) {
+  const int4 v = __ldg(&items[item]);
+  PfItem it;
+  it.shared = v.x < 0 ? 1 : 0;
+  it.e = v.x < 0 ? 0 : v.x;
+  it.m0 = v.y;
+  it.p0 = v.z;
+  it.cnt = v.w;
+  it.hpos0 = v.x < 0 ? p.T * p.k + v.z : v.z;
   return it;
 }
 
@@ -226,47 +257,47 @@ __device__ __forceinline__ int row_smax_part(const uint8_t* srow, int nwords, in
 }
 __device__ __forceinline__ int sigma_from_smax(int smax) { return smax < 0 ? 0 : 140 - smax; }
 
-// One MX block (32 elements: 16 bytes of codes, one scale byte) of weight row
-// r -> four 16-byte f16 chunks c0..c0+3 of the row in a SW128 tile, scaled by
-// 2^sigma.
-__device__ __forceinline__ void dq_mx_block(uint8_t* tile, uint32_t r, uint32_t c0, uint4 q, uint32_t s, int sigma) {
-  const uint32_t mul16 = s == 255u ? 0x7E00u : f16_pow2((int)s - 127 + sigma);
-  const uint32_t mul2 = mul16 | (mul16 << 16);
-  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+// 64 E2M1 codes of one weight row (q0: elements 0-31 = MX block 2s, q1:
+// elements 32-63 = block 2s + 1, scale bytes s0, s1) -> 32 f16x2 words in K
+// order (word c holds elements 2c, 2c + 1), scaled by 2^(e - 127 + sigma):
+// one exact conversion of two codes and one exact f16x2 multiply per word
+// (the row shift keeps every product in the f16 normal range).
+__device__ __forceinline__ void dq_row_mx(uint4 q0, uint4 q1, uint32_t s0, uint32_t s1, int sigma,
+                                          uint32_t (&o)[32]) {
+  uint32_t m0 = s0 == 255u ? 0x7E00u : f16_pow2((int)s0 - 127 + sigma);
+  uint32_t m1 = s1 == 255u ? 0x7E00u : f16_pow2((int)s1 - 127 + sigma);
+  m0 |= m0 << 16;
+  m1 |= m1 << 16;
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-  for (int wd = 0; wd < 4; ++wd) {
-    uint32_t o[4];
+  for (int wd = 0; wd < 8; ++wd)
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t w2 = e2m1x2_f16x2(words[wd], b);
-      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[b]) : "r"(w2), "r"(mul2));
+    for (int bt = 0; bt < 4; ++bt) {
+      const uint32_t c2 = e2m1x2_f16x2(w[wd], bt);
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * wd + bt]) : "r"(c2), "r"(wd < 4 ? m0 : m1));
     }
-    *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0 + wd)) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
 }
 
-// 32 bf16 weights (four 16-byte loads) -> four f16 chunks, scaled by `scale`
-// (a power of two).
-__device__ __forceinline__ void dq_bf16_block(uint8_t* tile, uint32_t r, uint32_t c0, const uint4 (&v)[4],
-                                              float scale) {
+// 64 bf16 weights of one row (eight 16-byte loads) -> 32 f16x2 words, scaled
+// by `scale` (a power of two).
+__device__ __forceinline__ void dq_row_bf16(const uint16_t* src, float scale, uint32_t (&o)[32]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-    uint32_t o[4];
+  for (int j = 0; j < 8; ++j) {
+    const uint4 v = ldg_stream(src + j * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const __half2 h2 =
           __floats2half2_rn(__uint_as_float(w[i] << 16) * scale, __uint_as_float(w[i] & 0xFFFF0000u) * scale);
-      o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0 + j)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 // -------------------------------------------------------- CTA control --
 struct PfShared {
-  uint64_t a_full[kPfMaxStages];   // weight tile stage filled: the 8 warps of one dequant group
-  uint64_t a_empty[kPfMaxStages];  // ... consumed: tcgen05.commit
+  uint64_t a_full[kPfMaxStages];   // A stage written to TMEM: the GW warps of one dequant group
+  uint64_t a_empty[kPfMaxStages];  // ... consumed: tcgen05.commit of each issuer
   uint64_t b_full[kPfMaxStages];   // token tile stage filled: 128 loader threads (cp.async arrivals)
   uint64_t b_empty[kPfMaxStages];  // ... consumed: tcgen05.commit
   uint64_t accf[2];              // accumulator buffer ready: tcgen05.commit of each issuer
@@ -280,15 +311,20 @@ struct PfShared {
   int col_tok[kPfEpWarps][kPfNTile];      // per epilogue warp: token of each column (down)
 };
 
-// Bounded wait that also gives up as soon as another role has aborted.  The
-// waiting thread sleeps in try_wait (at most kPfSleepNs per call) instead of
-// spinning: each SM sub-partition hosts waiting warps of several roles.
-constexpr uint32_t kPfSleepNs = 20000;
-__device__ __forceinline__ bool pf_wait(PfShared& sh, uint64_t* bar, uint32_t parity, WsHeader* hdr) {
+// Bounded wait that also gives up as soon as another role has aborted.
+// Between polls the waiting warp sleeps for `backoff_ns` (nanosleep: it
+// issues nothing meanwhile), so that waiting warps leave the issue slots to
+// the warps doing work; the roles on the tensor core's critical path poll
+// without sleeping, the others with longer sleeps the longer their waits
+// usually are.
+constexpr uint32_t kPfPollMma = 0, kPfPollDq = 32, kPfPollSig = 64, kPfPollLd = 128, kPfPollEp = 256;
+__device__ __forceinline__ bool pf_wait(PfShared& sh, uint64_t* bar, uint32_t parity, WsHeader* hdr,
+                                        uint32_t backoff_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, kPfSleepNs)) return true;
+    if (backoff_ns) __nanosleep(backoff_ns);
+    if (mbar_try_wait(bar, parity)) return true;
     if (*(volatile int*)&sh.abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       set_status(hdr, MOE_ERR_TIMEOUT);
@@ -301,211 +337,212 @@ __device__ __forceinline__ bool pf_wait(PfShared& sh, uint64_t* bar, uint32_t pa
 // Shared pipeline state of the four roles of one CTA.
 struct PfCtx {
   PfShared* sh;
-  uint8_t* smem_a;   // weight tile ring (NA tiles per stage), 1024-byte aligned
   uint8_t* smem_b;   // token tile ring, 1024-byte aligned
-  uint8_t* raw;      // raw MXFP4 ring of the dequant threads
+  uint8_t* raw;      // raw MXFP4 slots of the dequant groups
   int a_stages, b_stages;
-  int a_bytes;       // bytes of one weight tile stage
   int n_items;       // routed + shared items
   int n_routed;
   int U;
   const int32_t* pref;
+  const int4* items;  // this GEMM's item table
   int K, M, nslices;
   WsHeader* hdr;
 };
 
 // All lanes of a warp wait; the warp proceeds only if every lane succeeded.
-__device__ __forceinline__ bool pf_warp_wait(const PfCtx& c, uint64_t* bar, uint32_t parity) {
-  const bool ok = pf_wait(*c.sh, bar, parity, c.hdr);
+__device__ __forceinline__ bool pf_warp_wait(const PfCtx& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
+  const bool ok = pf_wait(*c.sh, bar, parity, c.hdr, backoff_ns);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Claim the ring stage of global slice gs for writing (wait until its
 // previous use was consumed by the tensor core).
-__device__ __forceinline__ bool pf_claim(const PfCtx& c, uint64_t* empty, int nstages, int gs) {
+__device__ __forceinline__ bool pf_claim(const PfCtx& c, uint64_t* empty, int nstages, int gs, uint32_t backoff_ns) {
   const int st = gs % nstages, use = gs / nstages;
   if (use == 0) return true;
-  return pf_warp_wait(c, &empty[st], (use - 1) & 1);
+  return pf_warp_wait(c, &empty[st], (use - 1) & 1, backoff_ns);
 }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// Prefetch cursor of a dequant thread: walks the CTA's items slice by slice
-// ahead of the consumer and issues one cp.async group per slice into the raw
-// ring (an empty group for slices of the shared expert or past the end, so
-// group counts stay aligned with slices).  It also keeps the rows streaming
-// from DRAM in long runs: each weight row is prefetched into L2 in
-// kPfL2Window-byte windows eight slices ahead of the cursor, and the first
-// 512 bytes of the next item's rows near the end of the current item (the
-// per-slice copies alone read 32 bytes per row, which DRAM serves poorly).
-template <int NA>
-struct PfCursor {
-  int item, s;
-  bool mx;                 // this slice's item is a routed MXFP4 item with a valid row
-  const uint8_t* row[NA];  // codes of the row
-  const uint8_t* sw[NA];   // scale row (one 4-byte word covers two slices)
-};
+// Row shift sigma of weight row `row` of matrix `a` (gate/down 0, up 1) of an
+// item: routed MXFP4 rows from their E8M0 scales (sigma = 140 - max scale),
+// shared-expert rows from the pre-pass; 0 for a row outside the matrix or an
+// expert with a bad descriptor (flagged elsewhere, not read).
+template <bool GATEUP>
+__device__ __forceinline__ int pf_row_sigma(const ExpertParams& p, const PfCtx& c, const PfItem& it, int a,
+                                            int row) {
+  if (row >= c.M) return 0;
+  if (it.shared) return __ldg(&p.ws.shsig[GATEUP ? (a == 0 ? row : p.I + row) : 2 * p.I + row]);
+  const moe_expert ex = p.experts[it.e];
+  if (!expert_ptrs_ok(ex)) return 0;
+  const uint8_t* sc = GATEUP ? (a == 0 ? ex.gate.s : ex.up.s) : ex.down.s;
+  return sigma_from_smax(row_smax_part(sc + (size_t)row * (c.K / 32), c.K / 128, 0, 1));
+}
 
-// Codes of weight row m0 + r of matrix a of `item`; null unless it is a
-// routed item with a valid row.
+// Codes and scales of weight row m0 + r of matrix a of `item`; null unless it
+// is a routed item with a valid row.
 __device__ __forceinline__ const uint8_t* item_row_codes(const ExpertParams& p, const PfCtx& c, bool gateup, int item,
-                                                         uint32_t r, int a, const uint8_t** scales) {
+                                                         int r, int a, const uint8_t** scales) {
   if (item >= c.n_items) return nullptr;
-  const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
+  const PfItem it = pf_item(item, p, c.items);
   if (it.shared) return nullptr;
   const moe_expert ex = p.experts[it.e];
-  const int row = it.m0 + (int)r;
+  const int row = it.m0 + r;
   if (row >= c.M || !expert_ptrs_ok(ex)) return nullptr;
   const moe_mx_mat m = a == 0 ? (gateup ? ex.gate : ex.down) : ex.up;
   if (scales) *scales = m.s + (size_t)row * (c.K / 32);
   return m.q + (size_t)row * (c.K / 2);
 }
 
-// The matrix whose L2 prefetches this thread issues (-1: none).
-template <int NA>
-__device__ __forceinline__ int prefetch_matrix(int half) {
-  return NA == 2 ? half : (half == 0 ? 0 : -1);
+// Raw-copy cursor of a dequant thread (matrix a, row r): walks the CTA's
+// global slice sequence g = ci * nslices + s (ci: the CTA's ci-th item) over
+// the slices of its group (g = grp, grp + NG, ...) ahead of the conversion
+// and issues one cp.async group per slice into the group's raw slots (an
+// empty group for the shared expert or past the end, so group counts stay
+// aligned with slices).  It also keeps the row streaming from DRAM in long
+// runs: the row is prefetched into L2 in kPfL2Window-byte windows eight
+// slices ahead, and the first 512 bytes of the next item's row near the end
+// of the current item (the per-slice copies alone read 32 bytes per row,
+// which DRAM serves poorly).
+struct PfCursor {
+  int g, ci;
+  const uint8_t* q;   // codes of the row (null: no MXFP4 copy)
+  const uint8_t* sw;  // scale row
+};
+
+__device__ __forceinline__ void cursor_enter(PfCursor& cur, const ExpertParams& p, const PfCtx& c, bool gateup,
+                                             int r, int a) {
+  cur.q = item_row_codes(p, c, gateup, blockIdx.x + cur.ci * (int)gridDim.x, r, a, &cur.sw);
 }
 
-template <int NA>
-__device__ __forceinline__ void cursor_enter(PfCursor<NA>& cur, const ExpertParams& p, const PfCtx& c, bool gateup,
-                                             uint32_t r) {
-  cur.mx = true;
-#pragma unroll
-  for (int a = 0; a < NA; ++a) {
-    cur.row[a] = item_row_codes(p, c, gateup, cur.item, r, a, &cur.sw[a]);
-    cur.mx = cur.mx && cur.row[a] != nullptr;
-  }
-}
-
-// Issue the cursor's slice into slot j % R of the group's raw ring, then move
-// the cursor kPfDqGroups slices on (the group's next slice).
-template <int NA, int R>
-__device__ __forceinline__ void cursor_issue(PfCursor<NA>& cur, const ExpertParams& p, const PfCtx& c, bool gateup,
-                                             uint32_t r, int half, uint8_t* raw, int j) {
-  const int tid = threadIdx.x % kPfDqGroupThreads;
-  uint8_t* slot = raw + (size_t)(j % R) * PfRaw<NA>::kStage;
-  if (cur.item < c.n_items) {
-    const int ns = c.nslices;
+template <bool GATEUP>
+__device__ __forceinline__ void cursor_issue(PfCursor& cur, const ExpertParams& p, const PfCtx& c, int r, int a,
+                                             int tid, uint8_t* raw, int j) {
+  using C = PfCfg<GATEUP>;
+  uint8_t* slot = raw + (size_t)(j % C::R) * C::kStage;
+  const int ns = c.nslices;
+  if (blockIdx.x + cur.ci * (int)gridDim.x < c.n_items) {
+    const int s = cur.g - cur.ci * ns;
     const int rowbytes = c.K / 2;
-    const int pa = prefetch_matrix<NA>(half);
-    if (cur.mx) {
-      if (pa >= 0 && (cur.s & 7) == 0) {
-        const int off = (cur.s + 8) * 32;
-        if (off < rowbytes) prefetch_l2(cur.row[pa] + off, (uint32_t)min(kPfL2Window, rowbytes - off));
+    if (cur.q) {
+      if ((s & 7) == 0) {
+        const int off = (s + 8) * 32;
+        if (off < rowbytes) prefetch_l2(cur.q + off, (uint32_t)min(kPfL2Window, rowbytes - off));
       }
-#pragma unroll
-      for (int a = 0; a < NA; ++a) {
-        cp_async16(slot + a * (kPfDqGroupThreads * 16) + tid * 16, cur.row[a] + (size_t)cur.s * 32 + half * 16);
-        cp_async4(slot + PfRaw<NA>::kQ + a * (kPfDqGroupThreads * 4) + tid * 4, cur.sw[a] + (cur.s >> 1) * 4);
-      }
+      cp_async16(slot + tid * 16, cur.q + (size_t)s * 32);
+      cp_async16(slot + C::kThreads * 16 + tid * 16, cur.q + (size_t)s * 32 + 16);
+      cp_async4(slot + C::kQ + tid * 4, cur.sw + (s >> 1) * 4);
     }
-    if (pa >= 0 && cur.s == (ns > 16 ? ns - 16 : 0)) {
-      const uint8_t* nq = item_row_codes(p, c, gateup, cur.item + gridDim.x, r, pa, nullptr);
+    if (s >= ns - 16 && s < ns - 16 + C::NG) {
+      const uint8_t* nq = item_row_codes(p, c, GATEUP, blockIdx.x + (cur.ci + 1) * (int)gridDim.x, r, a, nullptr);
       if (nq) prefetch_l2(nq, (uint32_t)min(512, rowbytes));
     }
-    cur.s += kPfDqGroups;
-    if (cur.s >= ns) {
-      cur.s -= ns;
-      cur.item += gridDim.x;
-      cursor_enter(cur, p, c, gateup, r);
+    cur.g += C::NG;
+    if (cur.g >= (cur.ci + 1) * ns) {
+      cur.ci = cur.g / ns;
+      cursor_enter(cur, p, c, GATEUP, r, a);
     }
   }
   cp_async_commit();
 }
 
-// Dequant warps: group k (warps 8k .. 8k+7) converts the slices s of every
-// item with s % 2 == k; in a group, thread (row r, half) produces MX block
-// 2s + half of weight row m0 + r, for gate and up (GATEUP) or down.  Routed
-// MXFP4 rows come through the group's raw ring; the bf16 shared expert's rows
-// are loaded directly.  (The slice count per item, K / 64, is even.)
+// Dequant warps.  Warp w is in group w / GW; inside its group it converts
+// matrix a = (w % GW) / 4 (gate/down 0, up 1), TMEM lane quarter w % 4: thread
+// (lane l) owns weight row m0 + 32 * (w % 4) + l of every item.  For each of
+// its group's slices it converts the row's 64 elements of the slice into 32
+// f16x2 columns and stores them into the slice's A stage in Tensor Memory
+// (tcgen05.st, 32 lanes x 32 columns per warp), then signals the stage.
+// Routed MXFP4 rows arrive through the group's raw slots (cp.async); the bf16
+// shared expert's rows are loaded directly.
 template <bool GATEUP>
-__device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c) {
-  constexpr int NA = GATEUP ? 2 : 1;
-  constexpr int R = GATEUP ? kPfRawGateUp : kPfRawDown;
-  const int grp = threadIdx.x / kPfDqGroupThreads;
-  const int tid = threadIdx.x % kPfDqGroupThreads;
-  const int lane = threadIdx.x & 31;
-  const uint32_t r = (uint32_t)tid >> 1;
-  const int half = tid & 1;
-  const uint32_t c0 = (uint32_t)half * 4;
+__device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem) {
+  using C = PfCfg<GATEUP>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / C::GW;
+  const int a = (warp % C::GW) >> 2;
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;
+  const int tid = threadIdx.x % C::kThreads;
   const int ns = c.nslices;
   PfShared& sh = *c.sh;
-  uint8_t* raw = c.raw + (size_t)grp * R * PfRaw<NA>::kStage;
-  PfCursor<NA> cur;
-  cur.item = blockIdx.x;
-  cur.s = grp;
-  cursor_enter(cur, p, c, GATEUP, r);
-  if (grp == 0 && cur.mx && prefetch_matrix<NA>(half) >= 0)
-    prefetch_l2(cur.row[prefetch_matrix<NA>(half)], (uint32_t)min(512, c.K / 2));
-  for (int j = 0; j < R; ++j) cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, raw, j);
-  int j = 0, ci = 0;  // j: the group's slices consumed so far
+  uint8_t* raw = c.raw + (size_t)grp * C::R * C::kStage;
+  const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + kPfAccCols + (uint32_t)(a * 32);
+  PfCursor cur;
+  cur.g = grp;
+  cur.ci = grp / ns;
+  cursor_enter(cur, p, c, GATEUP, r, a);
+  for (int j = 0; j < C::R; ++j) cursor_issue<GATEUP>(cur, p, c, r, a, tid, raw, j);
+  int ci_cur = -1;
+  int sig_next = 0;  // next local item whose row-shift slot this warp consumes
   bool ok = true;
-  for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x, ++ci) {
-    const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
-    // Row shifts of this item, published by the epilogue warps.
-    const int slot = ci % kPfSigRing;
-    if (!pf_warp_wait(c, &sh.sig_full[slot], (ci / kPfSigRing) & 1)) break;
-    int sig[NA];
-#pragma unroll
-    for (int a = 0; a < NA; ++a) sig[a] = sh.sig[slot][a][r];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.sig_empty[slot]);
-    const uint16_t* wp[NA];
-    float scale[NA];
-    if (it.shared) {
-      const int row = it.m0 + (int)r;
-      const int rowc = row < c.M ? row : c.M - 1;
-#pragma unroll
-      for (int a = 0; a < NA; ++a) {
+  PfItem it{};
+  int sigma = 0;
+  float bscale = 1.f;
+  const uint16_t* wrow = nullptr;
+  for (int g = grp, j = 0;; g += C::NG, ++j) {
+    const int ci = g / ns;
+    const int item = blockIdx.x + ci * (int)gridDim.x;
+    if (item >= c.n_items) break;
+    const int s = g - ci * ns;
+    if (ci != ci_cur) {
+      ci_cur = ci;
+      it = pf_item(item, p, c.items);
+      // Row shifts of this item from the ring (and release of the slots of
+      // items this group has no slice of).
+      for (; sig_next <= ci && ok; ++sig_next) {
+        const int slot = sig_next % kPfSigRing;
+        if (!pf_warp_wait(c, &sh.sig_full[slot], (sig_next / kPfSigRing) & 1, kPfPollSig)) {
+          ok = false;
+          break;
+        }
+        if (sig_next == ci) sigma = sh.sig[slot][a][r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.sig_empty[slot]);
+      }
+      if (!ok) break;
+      if (it.shared) {
+        const int row = min(it.m0 + r, c.M - 1);
         const uint16_t* base = GATEUP ? (a == 0 ? p.sh_gate : p.sh_up) : p.sh_down;
-        wp[a] = base + (size_t)rowc * c.K + half * 32;
-        scale[a] = __int_as_float((sig[a] + 127) << 23);
+        wrow = base + (size_t)row * c.K;
+        bscale = __int_as_float((sigma + 127) << 23);
       }
     }
-    for (int s = grp; s < ns; s += kPfDqGroups, ++j) {
-      const int g = ci * ns + s;
-      cp_async_wait<R - 1>();  // this slice's group (empty for the shared expert)
-      uint8_t* base = c.smem_a + (size_t)(g % c.a_stages) * c.a_bytes;
-      if (!it.shared) {
-        const uint8_t* rs = raw + (size_t)(j % R) * PfRaw<NA>::kStage;
-        uint4 q[NA];
-        uint32_t sc[NA];
-        const int byte = ((s & 1) << 1) | half;
-#pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          q[a] = lds128(rs + a * (kPfDqGroupThreads * 16) + tid * 16);
-          sc[a] = (*reinterpret_cast<const uint32_t*>(rs + PfRaw<NA>::kQ + a * (kPfDqGroupThreads * 4) + tid * 4) >>
-                   (8 * byte)) & 0xFFu;
-        }
-        if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int a = 0; a < NA; ++a) dq_mx_block(base + a * kPfTileBytes, r, c0, q[a], sc[a], sig[a]);
-      } else {
-        // bf16 shared expert: 32 weights (64 bytes) per thread and slice.
-        uint4 w[NA][4];
-#pragma unroll
-        for (int a = 0; a < NA; ++a)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) w[a][jj] = ldg_stream(wp[a] + (size_t)s * kPfSliceK + jj * 8);
-        if (!pf_claim(c, sh.a_empty, c.a_stages, g)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int a = 0; a < NA; ++a) dq_bf16_block(base + a * kPfTileBytes, r, c0, w[a], scale[a]);
-      }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.a_full[g % c.a_stages]);
-      cursor_issue<NA, R>(cur, p, c, GATEUP, r, half, raw, j + R);
+    cp_async_wait<C::R - 1>();  // this slice's group (empty for the shared expert)
+    uint32_t o[32];
+    if (!it.shared) {
+      const uint8_t* rs = raw + (size_t)(j % C::R) * C::kStage;
+      const uint4 q0 = lds128(rs + tid * 16);
+      const uint4 q1 = lds128(rs + C::kThreads * 16 + tid * 16);
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(rs + C::kQ + tid * 4) >> (16 * (s & 1));
+      // A row not copied (bad descriptor: flagged) converts stale slot bytes;
+      // the epilogue discards that row's outputs.
+      dq_row_mx(q0, q1, sw & 0xFFu, (sw >> 8) & 0xFFu, sigma, o);
+    } else {
+      dq_row_bf16(wrow + (size_t)s * kPfSliceK, bscale, o);
     }
-    if (*(volatile int*)&sh.abort_flag) ok = false;
+    if (!pf_claim(c, sh.a_empty, C::AS, g, kPfPollDq)) break;
+    tc_fence_after();
+    tmem_st32(tbase + (uint32_t)((g % C::AS) * C::ACOLS), o);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.a_full[g % C::AS]);
+    cursor_issue<GATEUP>(cur, p, c, r, a, tid, raw, j + C::R);
+    if (*(volatile int*)&sh.abort_flag) {
+      ok = false;
+      break;
+    }
+  }
+  // Release the row-shift slots of the CTA's remaining items.
+  const int n_local = blockIdx.x < c.n_items ? (c.n_items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  for (; ok && sig_next < n_local; ++sig_next) {
+    const int slot = sig_next % kPfSigRing;
+    if (!pf_warp_wait(c, &sh.sig_full[slot], (sig_next / kPfSigRing) & 1, kPfPollSig)) break;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.sig_empty[slot]);
   }
   cp_async_wait<0>();
 }
@@ -525,7 +562,7 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
   bool ok = true;
   int gbase = 0;
   for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x, gbase += ns) {
-    const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
+    const PfItem it = pf_item(item, p, c.items);
     const int nmma = (it.cnt + 15) & ~15;
     const uint16_t* src[8];
     uint32_t dst[8];
@@ -554,7 +591,7 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
     }
     for (int s = 0; s < ns; ++s) {
       const int gs = gbase + s;
-      if (!pf_claim(c, c.sh->b_empty, c.b_stages, gs)) {
+      if (!pf_claim(c, c.sh->b_empty, c.b_stages, gs, kPfPollLd)) {
         ok = false;
         break;
       }
@@ -575,32 +612,18 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
 }
 
 // Row shifts of local item j (the CTA's j-th item) into the shift ring, by
-// the epilogue warps (thread = one weight row).  Routed rows: from the E8M0
-// scales (sigma = 140 - max scale); shared-expert rows: from the pre-pass.
+// the epilogue warps (thread = one weight row).
 template <bool GATEUP>
 __device__ __forceinline__ bool pf_publish_sig(const ExpertParams& p, const PfCtx& c, int j) {
   PfShared& sh = *c.sh;
   const int slot = j % kPfSigRing, use = j / kPfSigRing;
-  if (use > 0 && !pf_warp_wait(c, &sh.sig_empty[slot], (use - 1) & 1)) return false;
+  if (use > 0 && !pf_warp_wait(c, &sh.sig_empty[slot], (use - 1) & 1, kPfPollSig)) return false;
   const int item = blockIdx.x + j * gridDim.x;
-  const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
+  const PfItem it = pf_item(item, p, c.items);
   const int rl = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
   const int row = it.m0 + rl;
-  int s0 = 0, s1 = 0;
-  if (row < c.M) {
-    if (!it.shared) {
-      const moe_expert ex = p.experts[it.e];
-      if (expert_ptrs_ok(ex)) {
-        s0 = sigma_from_smax(row_smax_part((GATEUP ? ex.gate.s : ex.down.s) + (size_t)row * (c.K / 32), c.K / 128, 0, 1));
-        if (GATEUP) s1 = sigma_from_smax(row_smax_part(ex.up.s + (size_t)row * (c.K / 32), c.K / 128, 0, 1));
-      }
-    } else {
-      s0 = __ldg(&p.ws.shsig[GATEUP ? row : 2 * p.I + row]);
-      if (GATEUP) s1 = __ldg(&p.ws.shsig[p.I + row]);
-    }
-  }
-  sh.sig[slot][0][rl] = s0;
-  sh.sig[slot][1][rl] = s1;
+  sh.sig[slot][0][rl] = pf_row_sigma<GATEUP>(p, c, it, 0, row);
+  sh.sig[slot][1][rl] = GATEUP ? pf_row_sigma<GATEUP>(p, c, it, 1, row) : 0;
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.sig_full[slot]);
   return true;
@@ -608,12 +631,14 @@ __device__ __forceinline__ bool pf_publish_sig(const ExpertParams& p, const PfCt
 
 // Epilogue warps: warp q (= warp % 4) reads TMEM lanes 32q..32q+31, i.e.
 // weight rows m0 + 32q + lane, one fp32 column per token.
-//   gate/up: h[hpos0 + n][row] = f16(silu(g) * u), shifts removed;
-//   down:    out[token(n)][row] += weight(n) * y.
+//   gate/up: h[hpos0 + n][row] = silu(g) * u in fp32, shifts removed, and the
+//            largest |h| of each h row raised into hmax;
+//   down:    out[token(n)][row] += weight(n) * 2^-tau(n) * y.
 // Before each item they publish the row shifts of the item kPfSigRing - 1
 // places ahead, so the dequant warps never wait on the scale reads.
 template <bool GATEUP>
 __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem) {
+  using C = PfCfg<GATEUP>;
   const int q = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
   const int npairs = p.T * p.k;
@@ -625,14 +650,14 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
     bool ok = true;
     while (ok && published < n_local && published < ci + kPfSigRing) ok = pf_publish_sig<GATEUP>(p, c, published++);
     if (!ok) break;
-    const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
-    const int b = ci & 1;
+    const PfItem it = pf_item(item, p, c.items);
+    const int b = ci % C::ACCB, use = ci / C::ACCB;
     const int rl = q * 32 + lane;
     const int row = it.m0 + rl;
     bool valid = row < c.M;
     if (!it.shared) valid = valid && expert_ptrs_ok(p.experts[it.e]);
     const int slot = ci % kPfSigRing;
-    if (!pf_warp_wait(c, &sh.sig_full[slot], (ci / kPfSigRing) & 1)) break;
+    if (!pf_warp_wait(c, &sh.sig_full[slot], (ci / kPfSigRing) & 1, kPfPollSig)) break;
     const float rs0 = ldexpf(1.f, -sh.sig[slot][0][rl]);  // 2^-sigma of the row: gate (or down), up
     const float rs1 = ldexpf(1.f, -sh.sig[slot][1][rl]);
     __syncwarp();
@@ -657,9 +682,9 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
       col_scale[n] = GATEUP ? __ldg(&p.ws.xscale[t]) : wgt * __ldg(&p.ws.hscale[it.hpos0 + n]);
     }
     __syncwarp();
-    if (!pf_warp_wait(c, &sh.accf[b], (ci >> 1) & 1)) break;
+    if (!pf_warp_wait(c, &sh.accf[b], use & 1, kPfPollEp)) break;
     tc_fence_after();
-    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACCW);
     for (int c0 = 0; c0 < it.cnt; c0 += 16) {
       uint32_t g[16];
       tmem_ld16(tbase + (uint32_t)c0, g);
@@ -675,16 +700,16 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int n = c0 + i;
-          uint32_t a = 0u;
+          uint32_t av = 0u;
           if (valid && n < it.cnt) {
             const float xs = col_scale[n];
             const float gv = __uint_as_float(g[i]) * rs0 * xs;
             const float uv = __uint_as_float(u[i]) * rs1 * xs;
             const float hv = silu_f32(gv) * uv;
             hout[(size_t)(it.hpos0 + n) * p.I + row] = hv;
-            a = __float_as_uint(hv) & 0x7FFFFFFFu;
+            av = __float_as_uint(hv) & 0x7FFFFFFFu;
           }
-          const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, a);
+          const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, av);
           if (lane == i) habs = mx;
         }
         if (lane < 16 && c0 + lane < it.cnt && habs != 0u) atomicMax(&p.ws.hmax[it.hpos0 + c0 + lane], habs);
@@ -709,44 +734,44 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
 }
 
 // MMA issuers (lane 0 of warp 24, and of warp 25 in the gate/up kernel): per
-// item, wait for a free accumulator buffer, then per stage for the weight and
-// token tiles, issue 4 K = 16 MMAs M = 128 x N = round16(tokens) into
-// accumulator `which` (gate/up: matrix `which`; down: the one accumulator),
-// and release the stages with tcgen05.commit; each issuer's last commit of the
-// item counts towards the accumulator buffer being ready.  (Splitting the down
-// contraction into even and odd stages over two issuers gave wrong tiles and
-// a stalled wait in testing; it is not used.)
+// item, wait for a free accumulator buffer, then per slice for the A stage
+// (Tensor Memory) and the token tile (shared memory), issue 4 K = 16 MMAs
+// M = 128 x N = round16(tokens) with A read from Tensor Memory into
+// accumulator `which` (gate/up: matrix `which`; down: the item's buffer), and
+// release both stages with tcgen05.commit; each issuer's last commit of the
+// item counts towards the accumulator being ready.
 template <bool GATEUP>
 __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem, int which) {
+  using C = PfCfg<GATEUP>;
   if (!GATEUP && which != 0) return;
   PfShared& sh = *c.sh;
   const int ns = c.nslices;
   int ci = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
-    const PfItem it = pf_item(item, p, c.pref, c.U, c.n_routed);
-    const int b = ci & 1;
-    if (ci >= 2 && !pf_wait(sh, &sh.acce[b], ((ci >> 1) - 1) & 1, c.hdr)) break;
+    const PfItem it = pf_item(item, p, c.items);
+    const int b = ci % C::ACCB, use = ci / C::ACCB;
+    if (use >= 1 && !pf_wait(sh, &sh.acce[b], (use - 1) & 1, c.hdr, kPfPollMma)) break;
     tc_fence_after();
     const int nmma = (it.cnt + 15) & ~15;
     const uint32_t idesc = idesc_f16_f32(kPfMTile, nmma);
-    const uint32_t dcol = tmem + (uint32_t)(b * 256 + which * 128);
+    const uint32_t dcol = tmem + (uint32_t)(b * C::ACCW + (GATEUP ? which * 128 : 0));
     bool ok = true;
     bool first = true;
     for (int s = 0; s < ns; ++s) {
       const int gs = ci * ns + s;
-      const int sa = gs % c.a_stages, sb = gs % c.b_stages;
-      if (!pf_wait(sh, &sh.a_full[sa], (gs / c.a_stages) & 1, c.hdr) ||
-          !pf_wait(sh, &sh.b_full[sb], (gs / c.b_stages) & 1, c.hdr)) {
+      const int sa = gs % C::AS, sb = gs % c.b_stages;
+      if (!pf_wait(sh, &sh.a_full[sa], (gs / C::AS) & 1, c.hdr, kPfPollMma) ||
+          !pf_wait(sh, &sh.b_full[sb], (gs / c.b_stages) & 1, c.hdr, kPfPollMma)) {
         ok = false;
         break;
       }
       fence_async_smem();  // the token tile was written by cp.async (generic proxy)
       tc_fence_after();
-      const uint32_t abase = smem_u32(c.smem_a + (size_t)sa * c.a_bytes + (GATEUP ? which * kPfTileBytes : 0));
+      const uint32_t acol = tmem + kPfAccCols + (uint32_t)(sa * C::ACOLS + (GATEUP ? which * 32 : 0));
       const uint32_t bbase = smem_u32(c.smem_b + (size_t)sb * kPfTileBytes);
 #pragma unroll
       for (int kk = 0; kk < kPfSliceK / 16; ++kk) {
-        umma_f16(dcol, sdesc_sw128(abase + kk * 32), sdesc_sw128(bbase + kk * 32), idesc, first ? 0u : 1u);
+        umma_f16_ts(dcol, acol + (uint32_t)(kk * 8), sdesc_sw128(bbase + kk * 32), idesc, first ? 0u : 1u);
         first = false;
       }
       umma_commit(&sh.a_empty[sa]);
@@ -761,7 +786,7 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
   // Every MMA issued must have finished before TMEM is released.
   if (ci > 0) {
     const int last = ci - 1;
-    if (!mbar_wait(&sh.accf[last & 1], (last >> 1) & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
+    if (!mbar_wait(&sh.accf[last % C::ACCB], (last / C::ACCB) & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
   }
 }
 
@@ -769,9 +794,7 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
 // I), K = H, B = f16 activations; else A = down rows (M = H), K = I, B = h.
 template <bool GATEUP>
 __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
-  constexpr int NA = GATEUP ? 2 : 1;
-  constexpr int AS = GATEUP ? kPfAStagesGateUp : kPfAStagesDown;
-  constexpr int BS = GATEUP ? kPfBStagesGateUp : kPfBStagesDown;
+  using C = PfCfg<GATEUP>;
   extern __shared__ uint8_t pf_dyn[];
   __shared__ PfShared sh;
   const int warp = threadIdx.x >> 5;
@@ -780,12 +803,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    // gate/up: both issuers read every stage; down: one issuer per stage.
-    for (int s = 0; s < AS; ++s) {
-      mbar_init(&sh.a_full[s], kPfDqGroupWarps);
+    // gate/up: both issuers read every stage; down: one issuer.
+    for (int s = 0; s < C::AS; ++s) {
+      mbar_init(&sh.a_full[s], C::GW);
       mbar_init(&sh.a_empty[s], GATEUP ? kPfMmaWarps : 1);
     }
-    for (int s = 0; s < BS; ++s) {
+    for (int s = 0; s < C::BS; ++s) {
       mbar_init(&sh.b_full[s], kPfLdWarps * 32);
       mbar_init(&sh.b_empty[s], GATEUP ? kPfMmaWarps : 1);
     }
@@ -807,24 +830,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
 
   PfCtx c;
   c.sh = &sh;
-  c.smem_a = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_dyn) + 1023) & ~(uintptr_t)1023);
-  c.a_stages = AS;
-  c.b_stages = BS;
-  c.a_bytes = NA * kPfTileBytes;
-  c.smem_b = c.smem_a + (size_t)AS * c.a_bytes;
-  c.raw = c.smem_b + (size_t)BS * kPfTileBytes;
+  c.smem_b = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_dyn) + 1023) & ~(uintptr_t)1023);
+  c.a_stages = C::AS;
+  c.b_stages = C::BS;
+  c.raw = c.smem_b + (size_t)C::BS * kPfTileBytes;
   c.K = GATEUP ? p.H : p.I;
   c.M = GATEUP ? p.I : p.H;
   c.nslices = c.K / kPfSliceK;
   c.hdr = p.ws.hdr;
   c.U = (int)p.ws.hdr->n_active;
   c.pref = GATEUP ? p.ws.act_pref_gu : p.ws.act_pref_dn;
+  c.items = GATEUP ? p.ws.items_gu : p.ws.items_dn;
   c.n_routed = c.U > 0 ? __ldg(&c.pref[c.U]) : 0;
   const int m_tiles = (c.M + kPfMTile - 1) / kPfMTile;
   c.n_items = c.n_routed + (p.sh_gate ? m_tiles * ((p.T + kPfNTile - 1) / kPfNTile) : 0);
 
   if (warp < kPfDqWarps)
-    pf_dequant_role<GATEUP>(p, c);
+    pf_dequant_role<GATEUP>(p, c, tmem);
   else if (warp < kPfDqWarps + kPfLdWarps)
     pf_loader_role<GATEUP>(p, c);
   else if (warp < kPfMmaWarp)
@@ -843,6 +865,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
 
 bool prefill_supported(int H, int I) { return H % 128 == 0 && I % 128 == 0; }
 
+template <bool GATEUP>
+constexpr size_t pf_smem_bytes() {
+  using C = PfCfg<GATEUP>;
+  // Token tile ring + raw MXFP4 slots + alignment slack.
+  return (size_t)C::BS * kPfTileBytes + (size_t)C::NG * C::R * C::kStage + 1024;
+}
+
 cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   if (!p.x_bf16 || !prefill_supported(p.H, p.I)) return cudaErrorNotSupported;
   const int nsm = device_sm_count();
@@ -858,11 +887,11 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   if (!p.accumulate) {
     if ((err = cudaMemsetAsync(p.out, 0, (size_t)p.T * p.H * sizeof(float), s)) != cudaSuccess) return err;
   }
-  // Weight tile ring + token tile ring + raw MXFP4 ring + alignment slack.
-  const size_t gu_smem = (size_t)(kPfAStagesGateUp * 2 + kPfBStagesGateUp) * kPfTileBytes +
-                         (size_t)kPfDqGroups * kPfRawGateUp * PfRaw<2>::kStage + 1024;
-  const size_t dn_smem = (size_t)(kPfAStagesDown + kPfBStagesDown) * kPfTileBytes +
-                         (size_t)kPfDqGroups * kPfRawDown * PfRaw<1>::kStage + 1024;
+  k_pf_items<<<nsm, 256, 0, s>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  constexpr size_t gu_smem = pf_smem_bytes<true>();
+  constexpr size_t dn_smem = pf_smem_bytes<false>();
+  static_assert(gu_smem + sizeof(PfShared) <= 227 * 1024 && dn_smem + sizeof(PfShared) <= 227 * 1024, "smem");
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
   prof_before(MOE_STAGE_PF_GATEUP, s);
