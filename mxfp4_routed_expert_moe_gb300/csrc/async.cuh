@@ -73,6 +73,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait_for(bar, parity, kWaitCycles);
 }
 
+// As mbar_wait, but the warp sleeps `ns` nanoseconds between polls (issuing
+// nothing meanwhile): for waiting roles that share an SM sub-partition with
+// warps whose instruction issue bounds the kernel.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+
 // Contiguous global -> shared copy by the bulk-copy engine, completing
 // `bytes` of transaction count on `bar`.  dst, src 16-byte aligned; bytes a
 // multiple of 16.

@@ -369,6 +369,10 @@ static cudaError_t launch_decode_ldg(const ExpertParams& p, cudaStream_t s) {
 // (batches of more than 64 tokens) the pair list stays in the workspace,
 // where it only ever holds checked entries (see load_plan).
 constexpr int kMaxStages = 8;
+// Sleep between polls of the producer and reducer waits (ns): those warps
+// share sub-partitions with the consumer warps, whose issue rate bounds the
+// kernels.
+constexpr uint32_t kDecPollProducer = 64, kDecPollReducer = 32;
 constexpr int kPlanSmemPairs = kDecodeMaxT * kMaxK;
 constexpr int kMaxPairs = kDecodeBatchMaxT * kMaxK;  // routed pairs of a decode batch
 
@@ -474,7 +478,7 @@ __device__ void ring_produce(Ring& rs, uint8_t* data, int stages, uint32_t stage
   bool ok = true;
   for (int it = 0;; ++it) {
     const int s = it % stages, use = it / stages;
-    if (use > 0 && !mbar_wait(&rs.empty[s], (use - 1) & 1)) {
+    if (use > 0 && !mbar_wait_backoff(&rs.empty[s], (use - 1) & 1, kDecPollProducer)) {
       ok = false;
       break;
     }
@@ -1009,7 +1013,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
       const int s = it % stages, use = it / stages;
       const int item = it < n_mine ? beg + it : -1;
       if (lane == 0) {
-        if (use > 0 && !mbar_wait(&rs.empty[s], (use - 1) & 1)) ok = false;
+        if (use > 0 && !mbar_wait_backoff(&rs.empty[s], (use - 1) & 1, kDecPollProducer)) ok = false;
         if (ok && *(volatile int*)&rs.abort_flag) ok = false;
         if (ok) rs.item[s] = item;
       }
@@ -1062,7 +1066,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
     const int r = lane >> 2, c = 2 * (lane & 3);
     for (int pc = 0;; ++pc) {
       const int slot = pc & 1;
-      if (!mbar_wait(&rs.red_full[slot], (pc >> 1) & 1)) {
+      if (!mbar_wait_backoff(&rs.red_full[slot], (pc >> 1) & 1, kDecPollReducer)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         break;
@@ -1291,7 +1295,7 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
   if (warp == ncons_w) {  // reducer (+ combine)
     for (int pc = 0;; ++pc) {
       const int slot = pc & 1;
-      if (!mbar_wait(&rs.red_full[slot], (pc >> 1) & 1)) {
+      if (!mbar_wait_backoff(&rs.red_full[slot], (pc >> 1) & 1, kDecPollReducer)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         break;
