@@ -51,6 +51,7 @@ constexpr int kPfLdWarps = 4;            // warps 16-19
 constexpr int kPfEpWarps = 4;            // warps 20-23
 constexpr int kPfMmaWarp = kPfDqWarps + kPfLdWarps + kPfEpWarps;  // warps 24-25; 24 owns TMEM
 constexpr int kPfMmaWarps = 2;
+constexpr int kPfGuIssuers = 2;          // gate/up: one thread per matrix issues its MMAs (1: one thread both)
 constexpr int kPfThreads = (kPfMmaWarp + kPfMmaWarps) * 32;
 constexpr int kPfMaxStages = 8;
 constexpr int kPfL2Window = 256;         // bytes of each weight row prefetched into L2 at a time
@@ -74,11 +75,12 @@ struct PfCfg {
   static constexpr int NA = GATEUP ? 2 : 1;
   static constexpr int GW = 4 * NA;
   static constexpr int NG = kPfDqWarps / GW;
+  static constexpr int NI = GATEUP ? kPfGuIssuers : 1;  // MMA-issuing threads
   static constexpr int ACCB = GATEUP ? 1 : 2;
   static constexpr int ACCW = GATEUP ? 256 : 128;  // columns per accumulator buffer
   static constexpr int ACOLS = 32 * NA;
   static constexpr int AS = (int)(kPfTmemCols - kPfAccCols) / ACOLS;  // 4 or 8
-  static constexpr int BS = 6;
+  static constexpr int BS = 8;                      // (a power of two, as AS)
   static constexpr int R = GATEUP ? 3 : 4;
   // Raw slot: the 32 bytes of codes of each group thread (first 16 bytes of
   // every thread, then the second 16), then its 4-byte scale word.
@@ -88,6 +90,9 @@ struct PfCfg {
 };
 static_assert(kPfEpWarps == 4 && (kPfDqWarps + kPfLdWarps) % 4 == 0, "epilogue warps must cover lane quarters 0-3");
 static_assert(PfCfg<true>::AS <= kPfMaxStages && PfCfg<false>::AS <= kPfMaxStages, "A stages");
+static_assert((PfCfg<true>::AS & (PfCfg<true>::AS - 1)) == 0 && (PfCfg<false>::AS & (PfCfg<false>::AS - 1)) == 0 &&
+                  (PfCfg<true>::BS & (PfCfg<true>::BS - 1)) == 0 && PfCfg<true>::BS <= kPfMaxStages,
+              "ring depths are powers of two (stage and phase by mask and shift)");
 
 // ------------------------------------------------------------ pre-passes --
 // xh[t][h] = f16(x[t][h] * 2^sigma_t), xscale[t] = 2^-sigma_t (one CTA per token).
@@ -358,7 +363,7 @@ __device__ __forceinline__ bool pf_warp_wait(const PfCtx& c, uint64_t* bar, uint
 // Claim the ring stage of global slice gs for writing (wait until its
 // previous use was consumed by the tensor core).
 __device__ __forceinline__ bool pf_claim(const PfCtx& c, uint64_t* empty, int nstages, int gs, uint32_t backoff_ns) {
-  const int st = gs % nstages, use = gs / nstages;
+  const int st = (int)((unsigned)gs % (unsigned)nstages), use = (int)((unsigned)gs / (unsigned)nstages);
   if (use == 0) return true;
   return pf_warp_wait(c, &empty[st], (use - 1) & 1, backoff_ns);
 }
@@ -482,11 +487,17 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c, uint32_t 
   int sigma = 0;
   float bscale = 1.f;
   const uint16_t* wrow = nullptr;
+  int ci = grp / ns, s = grp - (grp / ns) * ns;  // item (CTA-local) and slice of global slice g
   for (int g = grp, j = 0;; g += C::NG, ++j) {
-    const int ci = g / ns;
+    if (j > 0) {
+      s += C::NG;
+      while (s >= ns) {
+        s -= ns;
+        ++ci;
+      }
+    }
     const int item = blockIdx.x + ci * (int)gridDim.x;
     if (item >= c.n_items) break;
-    const int s = g - ci * ns;
     if (ci != ci_cur) {
       ci_cur = ci;
       it = pf_item(item, p, c.items);
@@ -525,11 +536,11 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c, uint32_t 
     }
     if (!pf_claim(c, sh.a_empty, C::AS, g, kPfPollDq)) break;
     tc_fence_after();
-    tmem_st32(tbase + (uint32_t)((g % C::AS) * C::ACOLS), o);
+    tmem_st32(tbase + (uint32_t)(((unsigned)g % C::AS) * C::ACOLS), o);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.a_full[g % C::AS]);
+    if (lane == 0) mbar_arrive(&sh.a_full[(unsigned)g % C::AS]);
     cursor_issue<GATEUP>(cur, p, c, r, a, tid, raw, j + C::R);
     if (*(volatile int*)&sh.abort_flag) {
       ok = false;
@@ -591,11 +602,11 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
     }
     for (int s = 0; s < ns; ++s) {
       const int gs = gbase + s;
-      if (!pf_claim(c, c.sh->b_empty, c.b_stages, gs, kPfPollLd)) {
+      if (!pf_claim(c, c.sh->b_empty, PfCfg<GATEUP>::BS, gs, kPfPollLd)) {
         ok = false;
         break;
       }
-      uint8_t* btile = c.smem_b + (size_t)(gs % c.b_stages) * kPfTileBytes;
+      uint8_t* btile = c.smem_b + (size_t)((unsigned)gs % PfCfg<GATEUP>::BS) * kPfTileBytes;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (!use_chunk[j]) continue;
@@ -604,7 +615,7 @@ __device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
         else
           cp_async16_zfill(btile + dst[j], p.ws.xh, 0u);
       }
-      cp_async_mbar_arrive(&c.sh->b_full[gs % c.b_stages]);
+      cp_async_mbar_arrive(&c.sh->b_full[(unsigned)gs % PfCfg<GATEUP>::BS]);
     }
     if (*(volatile int*)&c.sh->abort_flag) ok = false;
   }
@@ -743,7 +754,8 @@ __device__ void pf_epilogue_role(const ExpertParams& p, const PfCtx& c, uint32_t
 template <bool GATEUP>
 __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem, int which) {
   using C = PfCfg<GATEUP>;
-  if (!GATEUP && which != 0) return;
+  if (which >= C::NI) return;
+  constexpr int MPT = C::NA / C::NI;  // matrices this issuer covers
   PfShared& sh = *c.sh;
   const int ns = c.nslices;
   int ci = 0;
@@ -754,26 +766,29 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
     tc_fence_after();
     const int nmma = (it.cnt + 15) & ~15;
     const uint32_t idesc = idesc_f16_f32(kPfMTile, nmma);
-    const uint32_t dcol = tmem + (uint32_t)(b * C::ACCW + (GATEUP ? which * 128 : 0));
+    const uint32_t dcol = tmem + (uint32_t)(b * C::ACCW + which * MPT * 128);
     bool ok = true;
     bool first = true;
     for (int s = 0; s < ns; ++s) {
       const int gs = ci * ns + s;
-      const int sa = gs % C::AS, sb = gs % c.b_stages;
-      if (!pf_wait(sh, &sh.a_full[sa], (gs / C::AS) & 1, c.hdr, kPfPollMma) ||
-          !pf_wait(sh, &sh.b_full[sb], (gs / c.b_stages) & 1, c.hdr, kPfPollMma)) {
+      const unsigned ug = (unsigned)gs;
+      const int sa = (int)(ug % C::AS), sb = (int)(ug % C::BS);
+      if (!pf_wait(sh, &sh.a_full[sa], (ug / C::AS) & 1, c.hdr, kPfPollMma) ||
+          !pf_wait(sh, &sh.b_full[sb], (ug / C::BS) & 1, c.hdr, kPfPollMma)) {
         ok = false;
         break;
       }
       fence_async_smem();  // the token tile was written by cp.async (generic proxy)
       tc_fence_after();
-      const uint32_t acol = tmem + kPfAccCols + (uint32_t)(sa * C::ACOLS + (GATEUP ? which * 32 : 0));
+      const uint32_t acol = tmem + kPfAccCols + (uint32_t)(sa * C::ACOLS + which * MPT * 32);
       const uint32_t bbase = smem_u32(c.smem_b + (size_t)sb * kPfTileBytes);
 #pragma unroll
-      for (int kk = 0; kk < kPfSliceK / 16; ++kk) {
-        umma_f16_ts(dcol, acol + (uint32_t)(kk * 8), sdesc_sw128(bbase + kk * 32), idesc, first ? 0u : 1u);
-        first = false;
-      }
+      for (int kk = 0; kk < kPfSliceK / 16; ++kk)
+#pragma unroll
+        for (int m = 0; m < MPT; ++m)
+          umma_f16_ts(dcol + (uint32_t)(m * 128), acol + (uint32_t)(m * 32 + kk * 8), sdesc_sw128(bbase + kk * 32),
+                      idesc, (first && kk == 0) ? 0u : 1u);
+      first = false;
       umma_commit(&sh.a_empty[sa]);
       umma_commit(&sh.b_empty[sb]);
     }
@@ -806,14 +821,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
     // gate/up: both issuers read every stage; down: one issuer.
     for (int s = 0; s < C::AS; ++s) {
       mbar_init(&sh.a_full[s], C::GW);
-      mbar_init(&sh.a_empty[s], GATEUP ? kPfMmaWarps : 1);
+      mbar_init(&sh.a_empty[s], C::NI);
     }
     for (int s = 0; s < C::BS; ++s) {
       mbar_init(&sh.b_full[s], kPfLdWarps * 32);
-      mbar_init(&sh.b_empty[s], GATEUP ? kPfMmaWarps : 1);
+      mbar_init(&sh.b_empty[s], C::NI);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sh.accf[b], GATEUP ? kPfMmaWarps : 1);
+      mbar_init(&sh.accf[b], C::NI);
       mbar_init(&sh.acce[b], kPfEpWarps);
     }
     for (int i = 0; i < kPfSigRing; ++i) {
