@@ -246,6 +246,21 @@ int moe_forward_static_scratch(const moe_shape* shape, const void* x, int x_dtyp
  * compiled runtime, "One native build and test graph"]. */
 int moe_wait_selftest(long long max_cycles, void* stream, int* status_out);
 
+/* Diagnostic of the device-side failure handling: every bounded wait of the
+ * layer's kernels on another part of the same CTA (copies landing, a ring
+ * stage freed, partial sums handed over) gives up after `cycles` SM clock
+ * cycles instead of the default (about 4e9 cycles, ~2 s), records
+ * MOE_ERR_TIMEOUT in the workspace status word and takes the kernel's abort
+ * path: the other roles of the CTA stop, copies already issued are drained
+ * and Tensor Memory is released before the CTA exits (those draining waits
+ * keep the default limit).  cycles = 0 restores the default; otherwise
+ * 1 <= cycles <= 4e9, else MOE_ERR_INVALID_ARG.  Process-wide, read when a
+ * call launches its kernels (not thread-safe, like the profiling hook).  The
+ * outputs of a call that timed out are unspecified.  No counterpart on the
+ * pages: a small limit lets tests make real waits of the product kernels run
+ * out, without faulting or hanging the GPU. */
+int moe_set_wait_limit(long long cycles);
+
 /* Synchronises `stream`, then reads the device status word of `ws` into
  * *status_out (MOE_OK if no kernel flagged a problem since the last call that
  * began with this workspace).  Returns MOE_ERR_CUDA if the synchronisation or

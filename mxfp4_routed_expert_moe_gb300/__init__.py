@@ -37,7 +37,7 @@ DECODE_AUTO_PAIRS_PER_EXPERT = 12  # MOE_DECODE_AUTO_PAIRS_PER_EXPERT
 # Every symbol the header declares (checked by the tests against the .so).
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_route", "moe_mxfp4_experts",
            "moe_forward", "moe_device_status", "moe_profile_events", "moe_forward_static_scratch",
-           "moe_wait_selftest", "moe_select_path")
+           "moe_wait_selftest", "moe_select_path", "moe_set_wait_limit")
 STATIC_SCRATCH_BYTES = 8 << 20
 
 STAGE_ROUTE, STAGE_GATEUP, STAGE_DOWN, STAGE_COMBINE, STAGE_PF_GATEUP, STAGE_PF_DOWN = 1, 2, 3, 4, 5, 6
@@ -84,6 +84,7 @@ def lib():
             L.moe_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
             L.moe_profile_events.argtypes = [i32, vp, vp]
             L.moe_wait_selftest.argtypes = [ctypes.c_longlong, vp, P(ctypes.c_int)]
+            L.moe_set_wait_limit.argtypes = [ctypes.c_longlong]
             L.moe_select_path.argtypes = [P(Shape), i32, i32, i32, P(ctypes.c_int)]
             L.moe_forward_static_scratch.argtypes = [P(Shape), vp, i32, vp, vp, vp, P(DenseBf16), vp, i32, vp, vp,
                                                      i32, vp, vp]
@@ -210,6 +211,12 @@ def profile_events(stage: int, before=None, after=None) -> None:
     b = None if before is None else before.cuda_event
     a = None if after is None else after.cuda_event
     _check(lib().moe_profile_events(int(stage), b, a), "moe_profile_events")
+
+
+def set_wait_limit(cycles: int) -> None:
+    """moe_set_wait_limit: SM clock cycles after which the kernels' bounded
+    waits give up (diagnostic; 0 restores the default)."""
+    _check(lib().moe_set_wait_limit(int(cycles)), "moe_set_wait_limit")
 
 
 def device_status(ws, stream=None) -> int:

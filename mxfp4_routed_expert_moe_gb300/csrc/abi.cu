@@ -15,6 +15,12 @@ ProfHook g_prof = {};
 }
 
 namespace {
+// Cycles before a bounded device wait gives up (moe_set_wait_limit; the
+// default only ends waits that can never complete).
+long long g_wait_limit = kWaitCycles;
+}  // namespace
+
+namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -101,6 +107,7 @@ RouteParams route_params(const moe_shape* s, const void* x, int x_dtype, const f
   p.offsets = offsets;
   p.sorted = sorted;
   p.want_buckets = 1;
+  p.wait_limit = g_wait_limit;
   p.ws = ws;
   return p;
 }
@@ -118,6 +125,7 @@ int do_route(const moe_shape* s, const void* x, int x_dtype, const float* wr, co
   p.offsets = offsets;
   p.sorted = sorted;
   p.want_buckets = 1;
+  p.wait_limit = g_wait_limit;
   p.ws = ws;
   if (want_decode_route && route_decode_supported(s->T, s->H, s->E, s->k)) return cuda_status(launch_route_decode(p, st));
   return cuda_status(launch_route_prefill(p, bucket_params(s, ids, offsets, sorted, ws), st));
@@ -138,6 +146,7 @@ ExpertParams expert_params(const moe_shape* s, const void* x, int x_dtype, const
   p.sorted = sorted;
   p.out = out;
   p.accumulate = accumulate ? 1 : 0;
+  p.wait_limit = g_wait_limit;
   if (shared) {
     p.sh_gate = shared->gate;
     p.sh_up = shared->up;
@@ -346,6 +355,12 @@ int moe_wait_selftest(long long max_cycles, void* stream, int* status_out) {
       cudaStreamSynchronize(s) != cudaSuccess)
     return MOE_ERR_CUDA;
   *status_out = v;
+  return MOE_OK;
+}
+
+int moe_set_wait_limit(long long cycles) {
+  if (cycles < 0 || cycles > kWaitCycles) return MOE_ERR_INVALID_ARG;
+  g_wait_limit = cycles == 0 ? kWaitCycles : cycles;
   return MOE_OK;
 }
 

@@ -57,9 +57,32 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// A limit below the default is a diagnostic one (the library's
+// moe_set_wait_limit): the wait then polls with non-blocking tests, so that
+// the limit, not a suspended try_wait, is what ends it.
+__device__ __forceinline__ bool mbar_wait_diag(uint64_t* bar, uint32_t parity, long long max_cycles) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (clock64() - t0 > max_cycles) return false;
+  }
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // max_cycles SM clock cycles; false on timeout.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, long long max_cycles) {
+  if (max_cycles < kWaitCycles) return mbar_wait_diag(bar, parity, max_cycles);
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
@@ -76,13 +99,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // As mbar_wait, but the warp sleeps `ns` nanoseconds between polls (issuing
 // nothing meanwhile): for waiting roles that share an SM sub-partition with
 // warps whose instruction issue bounds the kernel.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t ns) {
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t ns,
+                                                  long long max_cycles = kWaitCycles) {
+  if (max_cycles < kWaitCycles) return mbar_wait_diag(bar, parity, max_cycles);
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     __nanosleep(ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > max_cycles) return false;
   }
 }
 

@@ -323,6 +323,7 @@ struct RouteParams {
   int32_t* offsets;     // bucket outputs (may alias workspace)
   int32_t* sorted;
   int want_buckets;
+  long long wait_limit;  // cycles before a bounded wait gives up (kWaitCycles unless diagnosing)
   Ws ws;
 };
 
@@ -355,6 +356,7 @@ struct ExpertParams {
   int shared_only;       // prefill kernels: the shared expert alone (decode path), no routed h rows
   int fused_route;       // decode: the gate/up kernel routes (from ws.logits) first
   RouteParams rp;        // the route to compute when fused_route
+  long long wait_limit;  // cycles before a bounded wait gives up (kWaitCycles unless diagnosing)
   Ws ws;
 };
 

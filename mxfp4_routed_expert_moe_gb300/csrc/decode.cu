@@ -472,13 +472,13 @@ __device__ void plan_cache_ptrs(const ExpertParams& p, Plan& pl, int which) {
 // consumers and drains its copies in flight before returning.
 template <typename NextItem, typename Issue>
 __device__ void ring_produce(Ring& rs, uint8_t* data, int stages, uint32_t stage_bytes, WsHeader* hdr,
-                             NextItem next_item, Issue issue) {
+                             long long wait_limit, NextItem next_item, Issue issue) {
   int issued_use[kMaxStages];
   for (int i = 0; i < kMaxStages; ++i) issued_use[i] = -1;
   bool ok = true;
   for (int it = 0;; ++it) {
     const int s = it % stages, use = it / stages;
-    if (use > 0 && !mbar_wait_backoff(&rs.empty[s], (use - 1) & 1, kDecPollProducer)) {
+    if (use > 0 && !mbar_wait_backoff(&rs.empty[s], (use - 1) & 1, kDecPollProducer, wait_limit)) {
       ok = false;
       break;
     }
@@ -490,6 +490,7 @@ __device__ void ring_produce(Ring& rs, uint8_t* data, int stages, uint32_t stage
     rs.item[s] = item;
     if (item < 0) {
       mbar_arrive(&rs.full[s]);
+      issued_use[s] = use;
       break;
     }
     issue(item, data + (size_t)s * stage_bytes, &rs.full[s]);
@@ -498,9 +499,12 @@ __device__ void ring_produce(Ring& rs, uint8_t* data, int stages, uint32_t stage
   if (!ok) {
     set_status(hdr, MOE_ERR_TIMEOUT);
     rs.abort_flag = 1;
-    for (int s = 0; s < stages; ++s)
-      if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
   }
+  // Before the CTA may exit, every copy issued has landed: wait for the last
+  // phase this producer started on each stage (complete at once in a normal
+  // run; bounded by the default limit).
+  for (int s = 0; s < stages; ++s)
+    if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
 }
 
 // h between the staged gate/up and down kernels is stored block-interleaved:
@@ -625,7 +629,7 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
 
   if (warp == ncons_w + 1) {  // producer
     if (lane == 0)
-      ring_produce(rs, ring_data, stages, stage_bytes, p.ws.hdr,
+      ring_produce(rs, ring_data, stages, stage_bytes, p.ws.hdr, p.wait_limit,
                    [&]() {
                      const int item = (int)atomicAdd(&p.ws.hdr->queue[kQGateUp], 1u);
                      return item < n_items ? item : -1;
@@ -651,7 +655,7 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
   if (warp == ncons_w) {  // reducer
     for (int pc = 0;; ++pc) {
       const int slot = pc & 1;
-      if (!mbar_wait(&rs.red_full[slot], (pc >> 1) & 1)) {
+      if (!mbar_wait_for(&rs.red_full[slot], (pc >> 1) & 1, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         break;
@@ -691,7 +695,7 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
   int pc = 0;
   for (int it = 0;; ++it) {
     const int s = it % stages, use = it / stages;
-    if (!mbar_wait(&rs.full[s], use & 1)) {
+    if (!mbar_wait_for(&rs.full[s], use & 1, p.wait_limit)) {
       set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
       rs.abort_flag = 1;
       break;
@@ -782,7 +786,7 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
       }
       const float tot = warp_transpose_reduce<kGuTmaVals>(acc);
       const int slot = pc & 1;
-      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+      if (pc >= 2 && !mbar_wait_for(&rs.red_empty[slot], ((pc >> 1) - 1) & 1, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         dead = true;
@@ -810,6 +814,8 @@ __global__ void __launch_bounds__(576, 1) k_dec_gateup_tma(ExpertParams p, int s
   // Tell the reducer there is no more work.
   {
     const int slot = pc & 1;
+    // After an abort the reducer leaves on its own (its wait gives up).
+    if (*(volatile int*)&rs.abort_flag) return;
     if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
     if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
     __syncwarp();
@@ -1013,7 +1019,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
       const int s = it % stages, use = it / stages;
       const int item = it < n_mine ? beg + it : -1;
       if (lane == 0) {
-        if (use > 0 && !mbar_wait_backoff(&rs.empty[s], (use - 1) & 1, kDecPollProducer)) ok = false;
+        if (use > 0 && !mbar_wait_backoff(&rs.empty[s], (use - 1) & 1, kDecPollProducer, p.wait_limit)) ok = false;
         if (ok && *(volatile int*)&rs.abort_flag) ok = false;
         if (ok) rs.item[s] = item;
       }
@@ -1021,7 +1027,10 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
       if (!ok) break;
       uint64_t* bar = &rs.full[s];
       if (item < 0) {
-        if (lane == 0) mbar_arrive(bar);
+        if (lane == 0) {
+          mbar_arrive(bar);
+          issued_use[s] = use;
+        }
         break;
       }
       const int u = item / tiles, rt = item % tiles;
@@ -1036,7 +1045,10 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
         __syncwarp();
       }
       if (!pp[0]) {  // bad descriptor: flagged in the plan, not read
-        if (lane == 0) mbar_arrive(bar);
+        if (lane == 0) {
+          mbar_arrive(bar);
+          issued_use[s] = use;
+        }
         continue;
       }
       const size_t r0 = (size_t)rt * 8;
@@ -1052,9 +1064,13 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
         bulk_g2s(st + sc_off + (size_t)(lane - kGmRows) * 8 * nbH, pp[2 + lane - kGmRows] + r0 * nbH,
                  (uint32_t)(8 * nbH), bar);
     }
-    if (!ok && lane == 0) {
-      set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
-      rs.abort_flag = 1;
+    if (lane == 0) {
+      if (!ok) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+      }
+      // Every copy issued has landed before the CTA may exit (the last phase
+      // started on each stage; complete at once in a normal run).
       for (int s = 0; s < stages; ++s)
         if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
     }
@@ -1066,7 +1082,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
     const int r = lane >> 2, c = 2 * (lane & 3);
     for (int pc = 0;; ++pc) {
       const int slot = pc & 1;
-      if (!mbar_wait_backoff(&rs.red_full[slot], (pc >> 1) & 1, kDecPollReducer)) {
+      if (!mbar_wait_backoff(&rs.red_full[slot], (pc >> 1) & 1, kDecPollReducer, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         break;
@@ -1127,7 +1143,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
   int s = 0;
   uint32_t phase = 0u;
   for (;; s = s + 1 == stages ? 0 : s + 1, phase ^= s == 0 ? 1u : 0u) {
-    if (!mbar_wait(&rs.full[s], phase)) {
+    if (!mbar_wait_for(&rs.full[s], phase, p.wait_limit)) {
       set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
       rs.abort_flag = 1;
       break;
@@ -1169,7 +1185,7 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
                       QB, acc);
       }
       const int slot = pc & 1;
-      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+      if (pc >= 2 && !mbar_wait_for(&rs.red_empty[slot], ((pc >> 1) - 1) & 1, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         dead = true;
@@ -1195,6 +1211,8 @@ __global__ void __launch_bounds__((kGmMaxWarps + kGmProducers + 1) * 32, 1)
   // Tell the reducer there is no more work.
   {
     const int slot = pc & 1;
+    // After an abort the reducer leaves on its own (its wait gives up).
+    if (*(volatile int*)&rs.abort_flag) return;
     if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
     if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
     __syncwarp();
@@ -1265,7 +1283,7 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
 
   if (warp == ncons_w + 1) {  // producer
     if (lane == 0)
-      ring_produce(rs, ring_data, stages, stage_bytes, p.ws.hdr,
+      ring_produce(rs, ring_data, stages, stage_bytes, p.ws.hdr, p.wait_limit,
                    [&]() {
                      const int item = (int)atomicAdd(&p.ws.hdr->queue[kQDown], 1u);
                      return item < n_items ? item : -1;
@@ -1295,7 +1313,7 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
   if (warp == ncons_w) {  // reducer (+ combine)
     for (int pc = 0;; ++pc) {
       const int slot = pc & 1;
-      if (!mbar_wait_backoff(&rs.red_full[slot], (pc >> 1) & 1, kDecPollReducer)) {
+      if (!mbar_wait_backoff(&rs.red_full[slot], (pc >> 1) & 1, kDecPollReducer, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         break;
@@ -1358,7 +1376,7 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
   int pc = 0;
   for (int it = 0;; ++it) {
     const int s = it % stages, use = it / stages;
-    if (!mbar_wait(&rs.full[s], use & 1)) {
+    if (!mbar_wait_for(&rs.full[s], use & 1, p.wait_limit)) {
       set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
       rs.abort_flag = 1;
       break;
@@ -1416,7 +1434,7 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
           acc[r][i] = v;
         }
       const int slot = pc & 1;
-      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+      if (pc >= 2 && !mbar_wait_for(&rs.red_empty[slot], ((pc >> 1) - 1) & 1, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         dead = true;
@@ -1447,6 +1465,8 @@ __global__ void __launch_bounds__(448, 1) k_dec_down_tma(ExpertParams p, int sta
   }
   {
     const int slot = pc & 1;
+    // After an abort the reducer leaves on its own (its wait gives up).
+    if (*(volatile int*)&rs.abort_flag) return;
     if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
     if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
     __syncwarp();
@@ -1587,7 +1607,7 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
       const int s = it % stages, use = it / stages;
       const int item = it < n_mine ? beg + it : -1;
       if (lane == 0) {
-        if (use > 0 && !mbar_wait(&rs.empty[s], (use - 1) & 1)) ok = false;
+        if (use > 0 && !mbar_wait_for(&rs.empty[s], (use - 1) & 1, p.wait_limit)) ok = false;
         if (ok && *(volatile int*)&rs.abort_flag) ok = false;
         if (ok) rs.item[s] = item;
       }
@@ -1595,13 +1615,19 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
       if (!ok) break;
       uint64_t* bar = &rs.full[s];
       if (item < 0) {
-        if (lane == 0) mbar_arrive(bar);
+        if (lane == 0) {
+          mbar_arrive(bar);
+          issued_use[s] = use;
+        }
         break;
       }
       const int u = item / tiles, rt = item % tiles;
       const uint8_t* const* pp = pl.ptrs + u * 2;
       if (!pp[0]) {  // bad descriptor: flagged in the plan, not read
-        if (lane == 0) mbar_arrive(bar);
+        if (lane == 0) {
+          mbar_arrive(bar);
+          issued_use[s] = use;
+        }
         continue;
       }
       const size_t r0 = (size_t)rt * kDmRows;
@@ -1615,9 +1641,13 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
         bulk_g2s(st + (size_t)c * gstride, pp[0] + (r0 + (size_t)c * rpc) * qrow, (uint32_t)rpc * qrow, bar);
       if (lane == 31) bulk_g2s(st + sc_off, pp[1] + r0 * nbI, (uint32_t)(kDmRows * nbI), bar);
     }
-    if (!ok && lane == 0) {
-      set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
-      rs.abort_flag = 1;
+    if (lane == 0) {
+      if (!ok) {
+        set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
+        rs.abort_flag = 1;
+      }
+      // Every copy issued has landed before the CTA may exit (the last phase
+      // started on each stage; complete at once in a normal run).
       for (int s = 0; s < stages; ++s)
         if (issued_use[s] >= 0) mbar_wait(&rs.full[s], issued_use[s] & 1);
     }
@@ -1627,7 +1657,7 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
   if (warp == W + 1 || warp == W + 2) {  // reducers: reducer r takes the passes that use slot r
     const int slot = warp - (W + 1);
     for (int j = 0;; ++j) {
-      if (!mbar_wait(&rs.red_full[slot], j & 1)) {
+      if (!mbar_wait_for(&rs.red_full[slot], j & 1, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         break;
@@ -1687,7 +1717,7 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
   bool dead = false;
   for (int it = 0; !dead; ++it) {
     const int s = it % stages;
-    if (!mbar_wait(&rs.full[s], (it / stages) & 1)) {
+    if (!mbar_wait_for(&rs.full[s], (it / stages) & 1, p.wait_limit)) {
       set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
       rs.abort_flag = 1;
       break;
@@ -1776,7 +1806,7 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
         }
       }
       const int slot = pc & 1;
-      if (pc >= 2 && !mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1)) {
+      if (pc >= 2 && !mbar_wait_for(&rs.red_empty[slot], ((pc >> 1) - 1) & 1, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         rs.abort_flag = 1;
         dead = true;
@@ -1806,6 +1836,8 @@ __global__ void __launch_bounds__((kDmMaxWarps + 3) * 32, 1)
   // Tell both reducers there is no more work.
   for (int e = 0; e < 2; ++e, ++pc) {
     const int slot = pc & 1;
+    // After an abort the reducer leaves on its own (its wait gives up).
+    if (*(volatile int*)&rs.abort_flag) return;
     if (pc >= 2) mbar_wait(&rs.red_empty[slot], ((pc >> 1) - 1) & 1);
     if (warp == 0 && lane == 0) rmeta[slot].r0 = -1;
     __syncwarp();

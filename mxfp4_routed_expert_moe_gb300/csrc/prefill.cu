@@ -30,6 +30,10 @@
 // techniques that bought the 82x"]; a batch of positions sharing experts
 // [Deltafin's custom compiled runtime, "Complete target sequence tape"] is
 // what makes the contraction dense enough for tensor cores here.
+#include <cuda.h>
+#include <string.h>
+
+#include <mutex>
 #include <utility>
 
 #include "async.cuh"
@@ -324,14 +328,15 @@ struct PfShared {
 // usually are.
 constexpr uint32_t kPfPollMma = 0, kPfPollDq = 32, kPfPollSig = 64, kPfPollLd = 128, kPfPollEp = 256;
 __device__ __forceinline__ bool pf_wait(PfShared& sh, uint64_t* bar, uint32_t parity, WsHeader* hdr,
-                                        uint32_t backoff_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                        uint32_t backoff_ns, long long limit) {
+  const bool diag = limit < kWaitCycles;  // diagnostic limit: non-blocking probes (see mbar_wait_diag)
+  if (diag ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (backoff_ns) __nanosleep(backoff_ns);
-    if (mbar_try_wait(bar, parity)) return true;
+    if (diag ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*(volatile int*)&sh.abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_status(hdr, MOE_ERR_TIMEOUT);
       *(volatile int*)&sh.abort_flag = 1;
       return false;
@@ -352,11 +357,12 @@ struct PfCtx {
   const int4* items;  // this GEMM's item table
   int K, M, nslices;
   WsHeader* hdr;
+  long long wait_limit;  // cycles before a wait on another role gives up
 };
 
 // All lanes of a warp wait; the warp proceeds only if every lane succeeded.
 __device__ __forceinline__ bool pf_warp_wait(const PfCtx& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
-  const bool ok = pf_wait(*c.sh, bar, parity, c.hdr, backoff_ns);
+  const bool ok = pf_wait(*c.sh, bar, parity, c.hdr, backoff_ns, c.wait_limit);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -566,9 +572,48 @@ __device__ void pf_dequant_role(const ExpertParams& p, const PfCtx& c, uint32_t 
 // so the loader never waits for its own copies: it runs ahead as far as the
 // ring allows and each stage is ready as soon as its data is.
 template <bool GATEUP>
-__device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c) {
+__device__ void pf_loader_role(const ExpertParams& p, const PfCtx& c, const CUtensorMap* tmap_h) {
   const int l = threadIdx.x - kPfDqWarps * 32;  // 0..127
   const int ns = c.nslices;
+  if (!GATEUP) {
+    // down: the token tile of slice s is the box (x = 64 s, y = hpos0) of the
+    // f16 h rows, one tensor-map copy by the first loader thread; rows past
+    // the end of h read as zero.
+    if (l >= 32) return;
+    constexpr int BS = PfCfg<GATEUP>::BS;
+    int issued[BS];  // last use of each stage with a copy issued (-1: none)
+#pragma unroll
+    for (int i = 0; i < BS; ++i) issued[i] = -1;
+    int gs = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x) {
+      const PfItem it = pf_item(item, p, c.items);
+      for (int s = 0; s < ns; ++s, ++gs) {
+        if (!pf_claim(c, c.sh->b_empty, BS, gs, kPfPollLd)) {
+          ok = false;
+          break;
+        }
+        if (l == 0) {
+          const int st = (int)((unsigned)gs % BS);
+          uint64_t* bar = &c.sh->b_full[st];
+          mbar_arrive_expect_tx(bar, (uint32_t)kPfTileBytes);
+          tma_load_2d(c.smem_b + (size_t)st * kPfTileBytes, tmap_h, s * kPfSliceK, it.hpos0, bar);
+#pragma unroll
+          for (int i = 0; i < BS; ++i)
+            if (i == st) issued[i] = (int)((unsigned)gs / BS);
+        }
+        __syncwarp();
+      }
+      if (*(volatile int*)&c.sh->abort_flag) ok = false;
+    }
+    // Every copy issued has landed before the CTA may exit (immediate after a
+    // normal run: the MMA issuer waited for each of them).
+    if (l == 0)
+#pragma unroll
+      for (int i = 0; i < BS; ++i)
+        if (issued[i] >= 0 && !mbar_wait(&c.sh->b_full[i], issued[i] & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
+    return;
+  }
   const int npairs = p.T * p.k;
   bool ok = true;
   int gbase = 0;
@@ -762,7 +807,7 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.items);
     const int b = ci % C::ACCB, use = ci / C::ACCB;
-    if (use >= 1 && !pf_wait(sh, &sh.acce[b], (use - 1) & 1, c.hdr, kPfPollMma)) break;
+    if (use >= 1 && !pf_wait(sh, &sh.acce[b], (use - 1) & 1, c.hdr, kPfPollMma, c.wait_limit)) break;
     tc_fence_after();
     const int nmma = (it.cnt + 15) & ~15;
     const uint32_t idesc = idesc_f16_f32(kPfMTile, nmma);
@@ -773,12 +818,12 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
       const int gs = ci * ns + s;
       const unsigned ug = (unsigned)gs;
       const int sa = (int)(ug % C::AS), sb = (int)(ug % C::BS);
-      if (!pf_wait(sh, &sh.a_full[sa], (ug / C::AS) & 1, c.hdr, kPfPollMma) ||
-          !pf_wait(sh, &sh.b_full[sb], (ug / C::BS) & 1, c.hdr, kPfPollMma)) {
+      if (!pf_wait(sh, &sh.a_full[sa], (ug / C::AS) & 1, c.hdr, kPfPollMma, c.wait_limit) ||
+          !pf_wait(sh, &sh.b_full[sb], (ug / C::BS) & 1, c.hdr, kPfPollMma, c.wait_limit)) {
         ok = false;
         break;
       }
-      fence_async_smem();  // the token tile was written by cp.async (generic proxy)
+      if (GATEUP) fence_async_smem();  // the token tile was written by cp.async (generic proxy)
       tc_fence_after();
       const uint32_t acol = tmem + kPfAccCols + (uint32_t)(sa * C::ACOLS + which * MPT * 32);
       const uint32_t bbase = smem_u32(c.smem_b + (size_t)sb * kPfTileBytes);
@@ -808,7 +853,7 @@ __device__ void pf_mma_role(const ExpertParams& p, const PfCtx& c, uint32_t tmem
 // Persistent grouped GEMM, one CTA per SM.  GATEUP: A = gate and up rows (M =
 // I), K = H, B = f16 activations; else A = down rows (M = H), K = I, B = h.
 template <bool GATEUP>
-__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const __grid_constant__ CUtensorMap tmap_h) {
   using C = PfCfg<GATEUP>;
   extern __shared__ uint8_t pf_dyn[];
   __shared__ PfShared sh;
@@ -824,7 +869,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
       mbar_init(&sh.a_empty[s], C::NI);
     }
     for (int s = 0; s < C::BS; ++s) {
-      mbar_init(&sh.b_full[s], kPfLdWarps * 32);
+      mbar_init(&sh.b_full[s], GATEUP ? kPfLdWarps * 32 : 1);
       mbar_init(&sh.b_empty[s], C::NI);
     }
     for (int b = 0; b < 2; ++b) {
@@ -853,6 +898,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
   c.M = GATEUP ? p.I : p.H;
   c.nslices = c.K / kPfSliceK;
   c.hdr = p.ws.hdr;
+  c.wait_limit = p.wait_limit;
   c.U = (int)p.ws.hdr->n_active;
   c.pref = GATEUP ? p.ws.act_pref_gu : p.ws.act_pref_dn;
   c.items = GATEUP ? p.ws.items_gu : p.ws.items_dn;
@@ -863,7 +909,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
   if (warp < kPfDqWarps)
     pf_dequant_role<GATEUP>(p, c, tmem);
   else if (warp < kPfDqWarps + kPfLdWarps)
-    pf_loader_role<GATEUP>(p, c);
+    pf_loader_role<GATEUP>(p, c, &tmap_h);
   else if (warp < kPfMmaWarp)
     pf_epilogue_role<GATEUP>(p, c, tmem);
   else if ((threadIdx.x & 31) == 0)
@@ -879,6 +925,43 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p) {
 }
 
 bool prefill_supported(int H, int I) { return H % 128 == 0 && I % 128 == 0; }
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on the driver library); null if unavailable.
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Tensor map of the f16 h rows [rows][I] for the down GEMM's token tiles:
+// boxes of 64 elements (128 bytes) x 128 rows, 128-byte swizzle (the MMA's
+// K-major operand layout), out-of-range rows read as zero.
+cudaError_t encode_h16_map(CUtensorMap* m, void* base, int rows, int I) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kPfSliceK, (cuuint32_t)kPfNTile};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+}  // namespace
 
 template <bool GATEUP>
 constexpr size_t pf_smem_bytes() {
@@ -909,8 +992,11 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   static_assert(gu_smem + sizeof(PfShared) <= 227 * 1024 && dn_smem + sizeof(PfShared) <= 227 * 1024, "smem");
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
+  CUtensorMap tmap_h;
+  memset(&tmap_h, 0, sizeof tmap_h);
+  if ((err = encode_h16_map(&tmap_h, p.ws.h16, p.T * p.k + p.T, p.I)) != cudaSuccess) return err;
   prof_before(MOE_STAGE_PF_GATEUP, s);
-  k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(p);
+  k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(p, tmap_h);
   prof_after(MOE_STAGE_PF_GATEUP, s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   // f16 h rows for the down GEMM: the routed pairs' rows (none when the
@@ -922,7 +1008,7 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   prof_before(MOE_STAGE_PF_DOWN, s);
-  k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(p);
+  k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(p, tmap_h);
   prof_after(MOE_STAGE_PF_DOWN, s);
   return cudaGetLastError();
 }

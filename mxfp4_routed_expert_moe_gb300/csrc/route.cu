@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kRgThreads) k_router_gemv(RouteParams p) {
       }
     }
     if (!rows_ready) {
-      if (!mbar_wait(&bar, 0)) {
+      if (!mbar_wait_for(&bar, 0, p.wait_limit)) {
         set_status(p.ws.hdr, MOE_ERR_TIMEOUT);
         mbar_wait(&bar, 0);  // bounded drain of the copy in flight
         return;

@@ -148,6 +148,19 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Tensor-map (TMA) load of one 2-D box at element coordinates (x, y) of the
+// map into shared memory, completing the box's bytes of transaction count on
+// `bar`.  `map` is the generic address of a CUtensorMap (a __grid_constant__
+// kernel parameter); dst follows the map's swizzle (1024-byte aligned for
+// 128-byte swizzle); x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Bulk prefetch of global memory into L2 (no data returned to the SM).
 // addr 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void prefetch_l2(const void* addr, uint32_t bytes) {
