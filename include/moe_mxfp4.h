@@ -130,7 +130,7 @@ typedef enum {
 
 #define MOE_DECODE_MAX_T 64
 #define MOE_DECODE_BATCH_MAX_T 1024
-#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 12
+#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 10
 
 typedef struct { const uint8_t* q; const uint8_t* s; } moe_mx_mat;   /* see above */
 typedef struct { moe_mx_mat gate, up, down; } moe_expert;            /* six tensors */
