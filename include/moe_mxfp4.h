@@ -52,10 +52,12 @@
  *     run).  `shape` and `shared` point to HOST structs; `experts` points to a
  *     DEVICE array of E moe_expert descriptors.
  *   - Alignment: x, out, shared-expert tensors: 16 bytes; ws: 256 bytes;
- *     every expert tensor (q and s): 16 bytes; everything else: its element
- *     size.  Host-visible misalignment is MOE_ERR_INVALID_ARG; an expert
- *     descriptor (device memory) with a null or misaligned tensor is detected
- *     on the device (MOE_ERR_DEVICE_CHECK) and that expert is not read.
+ *     every expert tensor (q and s): 16 bytes, and on the prefill path the
+ *     gate and up codes (q) 32 bytes (they are read by tensor-map copies of
+ *     4-bit elements); everything else: its element size.  Host-visible
+ *     misalignment is MOE_ERR_INVALID_ARG; an expert descriptor (device
+ *     memory) with a null or misaligned tensor is detected on the device
+ *     (MOE_ERR_DEVICE_CHECK) and that expert is not read.
  *   - Asynchrony: calls enqueue kernels on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and return; there is no host synchronisation
  *     except in moe_device_status().  The calls make no CUDA allocation.
@@ -212,7 +214,7 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
  * device allocator to hand the library (or must not allocate while serving).
  *   - Limit: shapes with moe_workspace_bytes(shape) > MOE_STATIC_SCRATCH_BYTES
  *     are rejected with MOE_ERR_WORKSPACE before anything is launched (the
- *     pages' layer shape H = 7168, E = 896, k = 16, I = 1408 fits up to T = 14).
+ *     pages' layer shape H = 7168, E = 896, k = 16, I = 1408 fits up to T = 13).
  *   - Set-up: the first call on a device (that device current) looks up the
  *     scratch address once; a CUDA failure there returns MOE_ERR_CUDA.  If the
  *     caller records its work into a CUDA graph, make one call before

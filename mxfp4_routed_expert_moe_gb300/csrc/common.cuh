@@ -47,6 +47,11 @@ struct Ws {
   int4* items_dn;       // prefill down work items, the same fields
   uint16_t* xh;         // [T][H]  fp16 activations (prefill)
   float* xscale;        // [T]     2^-sigma_t of the fp16 activations
+  uint8_t* xp;          // [2][T*k][H] prefill: each routed pair's activations as two E4M3
+                        // terms, rows in bucket order (aliases y)
+  int32_t* pinv;        // [T*k] prefill: bucket position of each routed pair (-1: none)
+  void* tmaps;          // [E][2] prefill: tensor maps (128 bytes each) of the gate and up codes
+  float* x8scale;       // [T]     2^-tau_t of token t's E4M3 terms
   void* h;              // fp32 h: [T*k][I] (decode) or [T*k + T][I] (prefill; rows
                         // T*k.. hold the shared expert's h)
   uint16_t* h16;        // [T*k + T][I] prefill: f16 h scaled by 2^tau_row (aliases y)
@@ -112,6 +117,9 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   }
   ws.xh = (uint16_t*)take(T * H * 2);
   ws.xscale = (float*)take(T * 4);
+  ws.x8scale = (float*)take(T * 4);
+  ws.pinv = (int32_t*)take(T * k * 4);
+  ws.tmaps = (void*)take(E * 2 * 128);
   // Tokens the decode path may take for this shape (0: it cannot).
   const size_t Td = T <= (size_t)kDecodeBatchMaxT ? T : 0;
   // h in fp32: Td*k rows for the decode path, T*k + T rows for the prefill
@@ -122,12 +130,17 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.hmax = (uint32_t*)take(hrows * 4);
   ws.hscale = (float*)take(hrows * 4);
   ws.shsig = (int32_t*)take((2 * I + H) * 4);
-  // y (decode) and the prefill path's f16 h share one region: the prefill
-  // kernels run on the decode path only for the shared expert, after the
-  // routed experts' combine has consumed y.
-  const size_t y_dec = Td * k * H * 4, h16_pf = hrows * I * 2;
-  ws.y = (float*)take(y_dec > h16_pf ? y_dec : h16_pf);
+  // y (decode), the prefill path's E4M3 activation rows and its f16 h share
+  // one region: the prefill kernels run on the decode path only for the
+  // shared expert, after the routed experts' combine has consumed y (and then
+  // without the E4M3 rows); on the prefill path the f16 h is written after
+  // the gate/up GEMM, the last reader of the E4M3 rows.
+  const size_t y_dec = Td * k * H * 4, h16_pf = hrows * I * 2, xp_pf = 2 * T * k * H;
+  size_t yreg = y_dec > h16_pf ? y_dec : h16_pf;
+  yreg = yreg > xp_pf ? yreg : xp_pf;
+  ws.y = (float*)take(yreg);
   ws.h16 = (uint16_t*)ws.y;
+  ws.xp = (uint8_t*)ws.y;
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
   const size_t S = (size_t)router_splits(s.T, s.E, s.H);
   ws.rpart = (float2*)take(S > 1 ? S * T * E * 8 : 0);

@@ -110,6 +110,91 @@ __global__ void __launch_bounds__(256) k_x_to_f16(ExpertParams p) {
   if (threadIdx.x == 0) p.ws.hmax[(size_t)p.T * p.k + t] = 0u;
 }
 
+// x[t] (bf16) as two E4M3 terms for the block-scaled gate/up GEMM: with
+// tau_t = 7 - floor(log2 max_h |x[t][h]|), v = x * 2^tau_t has its largest
+// magnitude in [128, 256); x1 = e4m3(v) (round to nearest even) keeps the top
+// 4 significant bits of v and x2 = e4m3(16 (v - x1)) the remaining 4 of a bf16
+// value, so v = x1 + x2 / 16 exactly for every element that is an E4M3 normal
+// number after scaling (|v| >= 2^-6, i.e. within 2^-13 of the maximum); below
+// that, the absolute error is at most 2^-14 (2^-21 of the maximum).
+// The terms are written once per routed pair of the token, at its bucket
+// position r = pinv[t k + j]: xp[0][r] = x1, xp[1][r] = x2 (one byte per
+// element, in h order), so that each GEMM item's token rows are contiguous;
+// x8scale[t] = 2^-tau_t.  One CTA per token; also clears the token's h-row
+// maxima.
+__global__ void __launch_bounds__(256) k_x_to_e4m3(ExpertParams p) {
+  __shared__ float wmax[8];
+  __shared__ int pos[32];
+  const int t = blockIdx.x, H = p.H, k = p.k;
+  if ((int)threadIdx.x < k) pos[threadIdx.x] = p.ws.pinv[(size_t)t * k + threadIdx.x];
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * H;
+  float m = 0.f;
+  for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xb + h);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
+  int tau = 0;
+  if (m > 0.f && m < INFINITY) tau = 7 - ((int)((__float_as_uint(m) >> 23) & 0xFF) - 127);
+  tau = tau > 126 ? 126 : (tau < -126 ? -126 : tau);
+  const float up = __int_as_float((tau + 127) << 23);
+  if (threadIdx.x == 0) p.ws.x8scale[t] = __int_as_float((127 - tau) << 23);
+  const size_t plane = (size_t)p.T * k * H;
+  for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xb + h);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o1[2], o2[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // Elements h + 2j (low bf16 half) and h + 2j + 1: the first goes to the
+      // low byte (cvt puts its first source operand in the high byte).
+      const float a = __uint_as_float(w[j] << 16) * up, b = __uint_as_float(w[j] & 0xFFFF0000u) * up;
+      unsigned short q1, q2;
+      uint32_t f2;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q1) : "f"(b), "f"(a));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f2) : "h"(q1));
+      const float2 x1f = __half22float2(*reinterpret_cast<const __half2*>(&f2));
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q2) : "f"((b - x1f.y) * 16.f), "f"((a - x1f.x) * 16.f));
+      const int wd = j >> 1, sh = 16 * (j & 1);
+      if ((j & 1) == 0) {
+        o1[wd] = q1;
+        o2[wd] = q2;
+      } else {
+        o1[wd] |= (uint32_t)q1 << sh;
+        o2[wd] |= (uint32_t)q2 << sh;
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = pos[j];
+      if (r < 0) continue;
+      uint8_t* x1 = p.ws.xp + (size_t)r * H + h;
+      *reinterpret_cast<uint2*>(x1) = make_uint2(o1[0], o1[1]);
+      *reinterpret_cast<uint2*>(x1 + plane) = make_uint2(o2[0], o2[1]);
+    }
+  }
+  if ((int)threadIdx.x < p.k) p.ws.hmax[(size_t)t * p.k + threadIdx.x] = 0u;
+  if (threadIdx.x == 0) p.ws.hmax[(size_t)p.T * p.k + t] = 0u;
+}
+
+// pinv[sorted[r]] = r for every bucket position r (entries outside [0, T k)
+// were flagged when the list was checked and are skipped here).
+__global__ void k_pf_pinv(ExpertParams p) {
+  const int n = p.T * p.k;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
+    const int pr = __ldg(&p.sorted[r]);
+    if (pr >= 0 && pr < n) p.ws.pinv[pr] = r;
+  }
+}
+
 // f16 copy of the fp32 h rows [row0, row1) for the down GEMM: row r is scaled
 // by 2^tau_r, tau_r = 14 - floor(log2 max|h_r|), which puts the row's largest
 // magnitude in [2^14, 2^15): no overflow, and every element within 2^28 of the
@@ -905,6 +990,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const
   c.n_routed = c.U > 0 ? __ldg(&c.pref[c.U]) : 0;
   const int m_tiles = (c.M + kPfMTile - 1) / kPfMTile;
   c.n_items = c.n_routed + (p.sh_gate ? m_tiles * ((p.T + kPfNTile - 1) / kPfNTile) : 0);
+  if (p.shared_only) {
+    // The shared expert's items alone (its routed items run elsewhere, or
+    // there are none).
+    c.items += c.n_routed;
+    c.n_items -= c.n_routed;
+    c.n_routed = 0;
+  }
 
   if (warp < kPfDqWarps)
     pf_dequant_role<GATEUP>(p, c, tmem);
@@ -921,6 +1013,430 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kPfTmemCols);
+  }
+}
+
+// --------------------------------------------- block-scaled gate/up GEMM --
+// The tensor core takes the MXFP4 weights as they are stored: tcgen05.mma
+// kind::mxf8f6f4 with A = E2M1 codes and their E8M0 block scales, and B = the
+// activations as two E4M3 terms (k_x_to_e4m3, rows in bucket order), scale
+// 2^0 for x1 and 2^-4 for x2.  Products are exact and accumulate in fp32 in Tensor Memory; nothing is
+// converted on CUDA cores and no operand passes through registers.  Work items
+// are those of k_pf_gemm (routed experts only); per 128-element slice of the
+// contraction (four MX blocks):
+//   * one producer thread loads the 128 gate and 128 up code rows with one
+//     tensor-map copy each (4-bit elements in the 16-codes-then-8-byte-gap
+//     layout the MMA reads, 128-byte swizzle; per-expert maps written by
+//     k_pf_mx_maps) and the item's token rows of both E4M3 terms, which are
+//     contiguous in bucket order, in boxes of 32 rows;
+//   * 4 scale warps (one per TMEM lane quarter) write the rows' scale words
+//     (4 bytes = the slice's four blocks) into the stage's scale columns;
+//   * one thread issues 16 MMAs (4 K-steps x gate/up x 2 terms, M = 128,
+//     N = round16(tokens), K = 32; the two terms share one read of A through
+//     the A collector) and releases the stage with tcgen05.commit;
+//   * 4 epilogue warps apply SwiGLU with the token's 2^-tau and store h in
+//     fp32 as k_pf_gemm does (with the h-row maxima for the f16 pass).
+// Code matrices must be 32-byte aligned for their tensor maps (checked: an
+// expert whose gate or up codes are not is flagged and skipped).
+namespace mxk {
+constexpr int kSliceK = 128;
+constexpr int kStages = 3;
+constexpr int kTile = 128 * 128;                // one 128-row operand tile (bytes)
+constexpr int kStageBytes = 4 * kTile;           // gate codes, up codes, x1, x2
+constexpr int kCodeTx = 128 * 64;                // bytes a code tile's copy delivers (4-bit codes)
+constexpr int kXBox = 32;                        // token rows per activation copy
+constexpr int kTmaWarp = 1;                      // warp 0: MMA issuer, owns TMEM
+constexpr int kSfWarp0 = 2, kSfWarps = 4;        // warps 2-5
+constexpr int kEpWarp0 = kSfWarp0 + kSfWarps, kEpWarps = 4;  // warps 6-9
+constexpr int kThreads = (kEpWarp0 + kEpWarps) * 32;
+// TMEM columns: gate accumulator [0, 128), up [128, 256); activation-term
+// scales [256, 260) = 2^0 and [260, 264) = 2^-4; weight scales of stage st,
+// matrix a at 264 + 8 st + 4 a.
+constexpr uint32_t kColSfb = 256, kColSfa = 264;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kColSfa + 8 * kStages <= kTmemCols, "TMEM columns");
+constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
+}  // namespace mxk
+
+struct MxShared {
+  uint64_t full[mxk::kStages];   // stage filled: producer (with the copies' bytes) + 4 scale warps
+  uint64_t empty[mxk::kStages];  // stage consumed: tcgen05.commit
+  uint64_t accf;                 // accumulators ready: tcgen05.commit
+  uint64_t acce;                 // accumulators drained: 4 epilogue warps
+  uint32_t tmem_base;
+  int abort_flag;
+  float col_scale[mxk::kEpWarps][kPfNTile];  // per epilogue warp: 2^-tau of each column's token
+};
+
+struct MxCtx {
+  MxShared* sh;
+  uint8_t* ring;  // kStages x kStageBytes, 1024-byte aligned
+  int n_items;
+  const int4* items;
+  int ns;  // slices per item
+  WsHeader* hdr;
+  long long wait_limit;
+};
+
+__device__ __forceinline__ bool mx_wait(const MxCtx& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
+  MxShared& sh = *c.sh;
+  const bool diag = c.wait_limit < kWaitCycles;
+  if (diag ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (backoff_ns) __nanosleep(backoff_ns);
+    if (diag ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*(volatile int*)&sh.abort_flag) return false;
+    if (clock64() - t0 > c.wait_limit) {
+      set_status(c.hdr, MOE_ERR_TIMEOUT);
+      *(volatile int*)&sh.abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mx_warp_wait(const MxCtx& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
+  const bool ok = mx_wait(c, bar, parity, backoff_ns);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+// Wait until ring stage gs % kStages is free for global slice gs.
+__device__ __forceinline__ bool mx_claim(const MxCtx& c, int gs, uint32_t backoff_ns) {
+  const int st = gs % mxk::kStages, use = gs / mxk::kStages;
+  if (use == 0) return true;
+  return mx_warp_wait(c, &c.sh->empty[st], (use - 1) & 1, backoff_ns);
+}
+
+// Gate and up code matrices usable by the tensor-map copies.
+__device__ __forceinline__ bool mx_codes_ok(const moe_expert& ex) {
+  return expert_ptrs_ok(ex) && (((uintptr_t)ex.gate.q | (uintptr_t)ex.up.q) & 31u) == 0;
+}
+
+// Tensor maps of the active experts' gate and up codes: the template (dims
+// H x I, row stride H / 2 bytes, box 128 x 128, 4-bit elements with 8-byte
+// gaps, 128-byte swizzle) with the expert's address.  Experts whose codes
+// cannot be mapped are flagged (MOE_ERR_DEVICE_CHECK) and get no map; the
+// GEMM skips their copies.  One thread per (active expert, matrix).
+__global__ void k_pf_mx_maps(ExpertParams p, const __grid_constant__ CUtensorMap tmpl) {
+  const int U = (int)p.ws.hdr->n_active;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * U; i += gridDim.x * blockDim.x) {
+    const int e = __ldg(&p.ws.act_e[i >> 1]);
+    const moe_expert ex = p.experts[e];
+    if (!mx_codes_ok(ex)) {
+      if ((i & 1) == 0) set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+      continue;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ws.tmaps) + (size_t)(2 * e + (i & 1)) * 128);
+    const uint4* src = reinterpret_cast<const uint4*>(&tmpl);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[j] = src[j];
+    const uint8_t* q = (i & 1) ? ex.up.q : ex.gate.q;
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(q) : "memory");
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  }
+}
+
+// Producer warp.  Per slice: claim the stage; lane 0 arms the stage's barrier
+// with the bytes of all copies and issues the two code-tile copies and the
+// token-row boxes of both terms (rows past the item's tokens belong to the
+// next bucket or read as zero: they only feed accumulator columns that the
+// epilogue ignores).  Its lane issues nothing else: the copy unit's queue is
+// what the tensor core waits on.
+__device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const CUtensorMap* xmap) {
+  const int lane = threadIdx.x & 31;
+  const int npairs = p.T * p.k;
+  MxShared& sh = *c.sh;
+  int gs = 0;
+  bool ok = true;
+  int issued[mxk::kStages];  // last use of each stage with copies issued (-1: none)
+#pragma unroll
+  for (int i = 0; i < mxk::kStages; ++i) issued[i] = -1;
+  for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x) {
+    const PfItem it = pf_item(item, p, c.items);
+    const moe_expert ex = p.experts[it.e];
+    const bool wok = mx_codes_ok(ex);
+    const int nbox = (it.cnt + mxk::kXBox - 1) / mxk::kXBox;
+    const uint8_t* maps = reinterpret_cast<const uint8_t*>(p.ws.tmaps) + (size_t)2 * it.e * 128;
+    if (wok && lane == 0) {
+      tmap_acquire(maps);
+      tmap_acquire(maps + 128);
+    }
+    const uint32_t tx = (wok ? 2u * mxk::kCodeTx : 0u) + 2u * (uint32_t)nbox * mxk::kXBox * mxk::kSliceK;
+    for (int s = 0; s < c.ns; ++s, ++gs) {
+      if (!mx_claim(c, gs, mxk::kPollTma)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const int st = gs % mxk::kStages;
+        uint8_t* sb = c.ring + (size_t)st * mxk::kStageBytes;
+        uint64_t* bar = &sh.full[st];
+        mbar_arrive_expect_tx(bar, tx);
+        if (wok) {
+          tma_load_2d(sb, maps, s * mxk::kSliceK, it.m0, bar);
+          tma_load_2d(sb + mxk::kTile, maps + 128, s * mxk::kSliceK, it.m0, bar);
+        }
+        for (int b = 0; b < nbox; ++b) {
+          const int y = it.p0 + b * mxk::kXBox;
+          tma_load_2d(sb + 2 * mxk::kTile + b * mxk::kXBox * 128, xmap, s * mxk::kSliceK, y, bar);
+          tma_load_2d(sb + 3 * mxk::kTile + b * mxk::kXBox * 128, xmap, s * mxk::kSliceK, npairs + y, bar);
+        }
+#pragma unroll
+        for (int i = 0; i < mxk::kStages; ++i)
+          if (i == st) issued[i] = gs / mxk::kStages;
+      }
+      __syncwarp();
+    }
+    if (*(volatile int*)&sh.abort_flag) ok = false;
+  }
+  // Every copy issued has landed before the CTA may exit (immediate after a
+  // normal run: the MMA issuer waited for each of them).
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < mxk::kStages; ++i)
+      if (issued[i] >= 0 && !mbar_wait(&sh.full[i], issued[i] & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
+}
+
+// Scale warps: warp quarter q writes, in lanes 32q..32q+31, the activation
+// terms' constant scales once, then per slice the scale words of gate and up
+// rows lane + 32 j (j = 0..3) into the stage's columns (the same words in
+// every quarter).  An expert that is skipped gets scale 1 (its rows are
+// discarded by the epilogue).  A slice reads 4 bytes of each scale row, so
+// the words are loaded kSfAhead slices ahead into a register ring, and the
+// rows are prefetched into L2 when an item starts (and the next item's
+// halfway through).
+constexpr int kSfAhead = 4;
+__device__ __forceinline__ void mx_prefetch_scale_rows(const ExpertParams& p, const MxCtx& c, int item, int r) {
+  if (item >= c.n_items) return;
+  const PfItem it = pf_item(item, p, c.items);
+  const moe_expert ex = p.experts[it.e];
+  if (!mx_codes_ok(ex)) return;
+  const size_t srow = (size_t)p.H / 32;
+  const uint8_t* rows[2] = {ex.gate.s + (size_t)(it.m0 + r) * srow, ex.up.s + (size_t)(it.m0 + r) * srow};
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+    for (size_t o = 0; o < srow; o += 128) prefetch_l2_line(rows[a] + o);
+#pragma unroll
+  for (int a = 0; a < 2; ++a) prefetch_l2_line(rows[a] + srow - 1);
+}
+
+__device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+  const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const uint32_t lbase = tmem + ((uint32_t)(q * 32) << 16);
+  tmem_st4(lbase + mxk::kColSfb, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  tmem_st4(lbase + mxk::kColSfb + 4, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
+  const size_t srow = (size_t)p.H / 32;  // scale bytes per row (a multiple of 4)
+  const size_t jstride = 32 * srow / 4;  // words between rows lane and lane + 32
+  int gs = 0;
+  bool ok = true;
+  mx_prefetch_scale_rows(p, c, blockIdx.x, q * 32 + lane);
+  for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x) {
+    const PfItem it = pf_item(item, p, c.items);
+    const moe_expert ex = p.experts[it.e];
+    const bool wok = mx_codes_ok(ex);
+    const uint32_t* sg = wok ? reinterpret_cast<const uint32_t*>(ex.gate.s + (size_t)(it.m0 + lane) * srow) : nullptr;
+    const uint32_t* su = wok ? reinterpret_cast<const uint32_t*>(ex.up.s + (size_t)(it.m0 + lane) * srow) : nullptr;
+    // Words of slice sl: w[0..3] gate rows lane + 32 j, w[4..7] up rows.
+    auto load = [&](uint32_t (&w)[8], int sl) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        w[j] = (wok && sl < c.ns) ? __ldg(sg + j * jstride + sl) : 0x7F7F7F7Fu;
+        w[4 + j] = (wok && sl < c.ns) ? __ldg(su + j * jstride + sl) : 0x7F7F7F7Fu;
+      }
+    };
+    uint32_t ring[kSfAhead][8];
+#pragma unroll
+    for (int i = 0; i < kSfAhead; ++i) load(ring[i], i);
+    for (int s0 = 0; s0 < c.ns && ok; s0 += kSfAhead) {
+#pragma unroll
+      for (int i = 0; i < kSfAhead; ++i) {
+        const int s = s0 + i;
+        if (s >= c.ns) break;
+        if (s == c.ns / 2) mx_prefetch_scale_rows(p, c, item + gridDim.x, q * 32 + lane);
+        if (!mx_claim(c, gs, mxk::kPollSf)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = gs % mxk::kStages;
+        tmem_st4(lbase + mxk::kColSfa + 8 * st, ring[i][0], ring[i][1], ring[i][2], ring[i][3]);
+        tmem_st4(lbase + mxk::kColSfa + 8 * st + 4, ring[i][4], ring[i][5], ring[i][6], ring[i][7]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.sh->full[st]);
+        ++gs;
+        load(ring[i], s + kSfAhead);
+      }
+    }
+    if (*(volatile int*)&c.sh->abort_flag) ok = false;
+  }
+  tmem_st_wait();
+}
+
+// MMA issuer (lane 0 of warp 0): per item, wait for the accumulators to be
+// drained, then per slice for the stage, issue the 16 MMAs and commit the
+// stage; after the last slice commit the accumulators.  The operands were
+// written by tensor-map copies (async proxy), so no proxy fence is needed.
+__device__ void mx_mma_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+  MxShared& sh = *c.sh;
+  int ci = 0, gs = 0;
+  for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
+    const PfItem it = pf_item(item, p, c.items);
+    if (ci >= 1 && !mx_wait(c, &sh.acce, (ci - 1) & 1, mxk::kPollMma)) break;
+    tc_fence_after();
+    const int nmma = (it.cnt + 15) & ~15;
+    const uint32_t ibase = idesc_mx_f32(kPfMTile, nmma, kMxE2M1, kMxE4M3, 0, 0);
+    bool ok = true;
+    for (int s = 0; s < c.ns; ++s, ++gs) {
+      const int st = gs % mxk::kStages;
+      if (!mx_wait(c, &sh.full[st], (gs / mxk::kStages) & 1, mxk::kPollMma)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sbase = smem_u32(c.ring + (size_t)st * mxk::kStageBytes);
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint32_t idesc = ibase | ((uint32_t)kb << 29) | ((uint32_t)kb << 4);
+        const uint64_t b1 = sdesc_sw128(sbase + 2 * mxk::kTile + 32 * kb);
+        const uint64_t b2 = sdesc_sw128(sbase + 3 * mxk::kTile + 32 * kb);
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const uint64_t ad = sdesc_sw128(sbase + a * mxk::kTile + 32 * kb);
+          const uint32_t d = tmem + (uint32_t)(a * 128);
+          const uint32_t sfa = tmem + mxk::kColSfa + (uint32_t)(8 * st + 4 * a);
+          umma_mx_fill(d, ad, b1, idesc, sfa, tmem + mxk::kColSfb, (s > 0 || kb > 0) ? 1u : 0u);
+          umma_mx_lastuse(d, ad, b2, idesc, sfa, tmem + mxk::kColSfb + 4, 1u);
+        }
+      }
+      umma_commit(&sh.empty[st]);
+    }
+    umma_commit(&sh.accf);
+    if (!ok) {
+      ++ci;
+      break;
+    }
+  }
+  // Every MMA issued must have finished before TMEM is released.
+  if (ci > 0 && !mbar_wait(&sh.accf, (ci - 1) & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
+}
+
+// Epilogue warps: warp q reads TMEM lanes 32q..32q+31 (weight rows m0 + 32q +
+// lane): h[hpos0 + n][row] = silu(g) * u with both scaled by the token's
+// 2^-tau, in fp32, raising each h row's largest |h| into hmax.  A row with a
+// NaN block scale (E8M0 code 255) in gate or up gives NaN, as the definition
+// of the format has it (checked here, while the item's MMAs run).
+__device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+  MxShared& sh = *c.sh;
+  const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int npairs = p.T * p.k;
+  const int nsw = p.H / 128;  // scale words per row
+  float* hout = reinterpret_cast<float*>(p.ws.h);
+  int ci = 0;
+  for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
+    const PfItem it = pf_item(item, p, c.items);
+    const int row = it.m0 + q * 32 + lane;
+    const moe_expert ex = p.experts[it.e];
+    const bool valid = mx_codes_ok(ex);
+    bool nan_row = false;
+    if (valid) {
+      const uint32_t* g = reinterpret_cast<const uint32_t*>(ex.gate.s + (size_t)row * (p.H / 32));
+      const uint32_t* u = reinterpret_cast<const uint32_t*>(ex.up.s + (size_t)row * (p.H / 32));
+      uint32_t any = 0u;
+#pragma unroll 8
+      for (int i = 0; i < nsw; ++i) {
+        const uint32_t a = __ldg(g + i), b = __ldg(u + i);
+        // A byte equal to 0xFF: all of its bits set (per-byte test without carries).
+        any |= (a & (a >> 1) & (a >> 2) & (a >> 3) & (a >> 4) & (a >> 5) & (a >> 6) & (a >> 7)) & 0x01010101u;
+        any |= (b & (b >> 1) & (b >> 2) & (b >> 3) & (b >> 4) & (b >> 5) & (b >> 6) & (b >> 7)) & 0x01010101u;
+      }
+      nan_row = any != 0u;
+    }
+    float* col_scale = sh.col_scale[q];
+    __syncwarp();
+    for (int n = lane; n < it.cnt; n += 32) {
+      int pr = __ldg(&p.sorted[it.p0 + n]);
+      if (pr < 0 || pr >= npairs) pr = 0;  // flagged by the producer
+      col_scale[n] = __ldg(&p.ws.x8scale[pr / p.k]);
+    }
+    __syncwarp();
+    if (!mx_warp_wait(c, &sh.accf, ci & 1, mxk::kPollEp)) break;
+    tc_fence_after();
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+    for (int c0 = 0; c0 < it.cnt; c0 += 16) {
+      uint32_t g[16], u[16];
+      tmem_ld16(tbase + (uint32_t)c0, g);
+      tmem_ld16(tbase + 128u + (uint32_t)c0, u);
+      tmem_ld_wait();
+      uint32_t habs = 0u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = c0 + i;
+        uint32_t av = 0u;
+        if (valid && n < it.cnt) {
+          const float xs = col_scale[n];
+          float hv = silu_f32(__uint_as_float(g[i]) * xs) * (__uint_as_float(u[i]) * xs);
+          if (nan_row) hv = __int_as_float(0x7FC00000);
+          hout[(size_t)(it.hpos0 + n) * p.I + row] = hv;
+          av = __float_as_uint(hv) & 0x7FFFFFFFu;
+        }
+        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, av);
+        if (lane == i) habs = mx;
+      }
+      if (lane < 16 && c0 + lane < it.cnt && habs != 0u) atomicMax(&p.ws.hmax[it.hpos0 + c0 + lane], habs);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.acce);
+  }
+}
+
+__global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx_gateup(ExpertParams p,
+                                                                   const __grid_constant__ CUtensorMap xmap) {
+  extern __shared__ uint8_t mx_dyn[];
+  __shared__ MxShared sh;
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, mxk::kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < mxk::kStages; ++s) {
+      mbar_init(&sh.full[s], 1 + mxk::kSfWarps);
+      mbar_init(&sh.empty[s], 1);
+    }
+    mbar_init(&sh.accf, 1);
+    mbar_init(&sh.acce, mxk::kEpWarps);
+    sh.abort_flag = 0;
+    mbar_init_fence();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  MxCtx c;
+  c.sh = &sh;
+  c.ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mx_dyn) + 1023) & ~(uintptr_t)1023);
+  const int U = (int)p.ws.hdr->n_active;
+  c.n_items = U > 0 ? __ldg(&p.ws.act_pref_gu[U]) : 0;
+  c.items = p.ws.items_gu;
+  c.ns = p.H / mxk::kSliceK;
+  c.hdr = p.ws.hdr;
+  c.wait_limit = p.wait_limit;
+  if (warp == 0) {
+    if ((threadIdx.x & 31) == 0) mx_mma_role(p, c, tmem);
+  } else if (warp == mxk::kTmaWarp) {
+    mx_producer_role(p, c, &xmap);
+  } else if (warp < mxk::kEpWarp0) {
+    mx_scale_role(p, c, tmem);
+  } else {
+    mx_epilogue_role(p, c, tmem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, mxk::kTmemCols);
   }
 }
 
@@ -961,6 +1477,39 @@ cudaError_t encode_h16_map(CUtensorMap* m, void* base, int rows, int I) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+// Template of the per-expert code maps of the block-scaled gate/up GEMM: an
+// [I][H] matrix of 4-bit codes (row stride H / 2 bytes), boxes of 128
+// elements x 128 rows, each 16 codes stored as 8 bytes followed by an 8-byte
+// gap, 128-byte swizzle.  `base` only has to be a valid 32-byte-aligned
+// address: k_pf_mx_maps replaces it per expert.
+cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int H, int I) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)I};
+  const cuuint64_t strides[1] = {(cuuint64_t)H / 2};
+  const cuuint32_t box[2] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)kPfMTile};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Map of the bucket-order E4M3 activation rows of both terms as one
+// [2 T k][H] byte matrix: boxes of 32 rows x 128 bytes, 128-byte swizzle;
+// rows past the end read as zero.
+cudaError_t encode_xp_map(CUtensorMap* m, void* base, int npairs, int H) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)2 * npairs};
+  const cuuint64_t strides[1] = {(cuuint64_t)H};
+  const cuuint32_t box[2] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)mxk::kXBox};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 }  // namespace
 
 template <bool GATEUP>
@@ -975,10 +1524,21 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   const int nsm = device_sm_count();
   cudaError_t err;
   // Bucket layout, active experts and tile prefixes come from the routing or
-  // bucketing kernels already on the stream.
-  k_x_to_f16<<<p.T, 256, 0, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  // bucketing kernels already on the stream.  Routed experts run on the
+  // block-scaled gate/up GEMM (E4M3 activation terms); the bf16 shared expert
+  // on k_pf_gemm (f16 activations).
+  const bool routed = !p.shared_only;
+  if (routed) {
+    // Bucket position of every routed pair, then the pairs' E4M3 rows.
+    if ((err = cudaMemsetAsync(p.ws.pinv, 0xFF, (size_t)p.T * p.k * 4, s)) != cudaSuccess) return err;
+    k_pf_pinv<<<(p.T * p.k + 255) / 256, 256, 0, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    k_x_to_e4m3<<<p.T, 256, 0, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   if (p.sh_gate) {
+    k_x_to_f16<<<p.T, 256, 0, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     k_shared_sigma<<<(2 * p.I + p.H + 7) / 8, 256, 0, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
@@ -987,18 +1547,35 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   }
   k_pf_items<<<nsm, 256, 0, s>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  constexpr size_t mx_smem = (size_t)mxk::kStages * mxk::kStageBytes + 1024;
   constexpr size_t gu_smem = pf_smem_bytes<true>();
   constexpr size_t dn_smem = pf_smem_bytes<false>();
   static_assert(gu_smem + sizeof(PfShared) <= 227 * 1024 && dn_smem + sizeof(PfShared) <= 227 * 1024, "smem");
+  static_assert(mx_smem + sizeof(MxShared) <= 227 * 1024, "smem");
+  if ((err = ensure_smem_attr((const void*)k_pf_mx_gateup, mx_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
-  CUtensorMap tmap_h;
+  CUtensorMap tmap_h, tmap_codes, tmap_xp;
   memset(&tmap_h, 0, sizeof tmap_h);
+  memset(&tmap_codes, 0, sizeof tmap_codes);
+  memset(&tmap_xp, 0, sizeof tmap_xp);
   if ((err = encode_h16_map(&tmap_h, p.ws.h16, p.T * p.k + p.T, p.I)) != cudaSuccess) return err;
+  if (routed) {
+    if ((err = encode_code_map_template(&tmap_codes, p.ws.tmaps, p.H, p.I)) != cudaSuccess) return err;
+    if ((err = encode_xp_map(&tmap_xp, p.ws.xp, p.T * p.k, p.H)) != cudaSuccess) return err;
+    k_pf_mx_maps<<<(2 * p.E + 255) / 256, 256, 0, s>>>(p, tmap_codes);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   prof_before(MOE_STAGE_PF_GATEUP, s);
-  k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(p, tmap_h);
+  if (routed) k_pf_mx_gateup<<<nsm, mxk::kThreads, mx_smem, s>>>(p, tmap_xp);
+  if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
+    ExpertParams ps = p;
+    ps.shared_only = 1;
+    k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(ps, tmap_h);
+    err = cudaGetLastError();
+  }
   prof_after(MOE_STAGE_PF_GATEUP, s);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   // f16 h rows for the down GEMM: the routed pairs' rows (none when the
   // shared expert runs alone) and the shared expert's.
   const int hrow0 = p.shared_only ? p.T * p.k : 0;

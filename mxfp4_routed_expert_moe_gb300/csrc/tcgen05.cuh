@@ -42,6 +42,17 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M >> 4
 }
 
+// Instruction descriptor, kind::mxf8f6f4 with UE8M0 block scales (one scale
+// per 32 elements of K): A and B K-major, D = f32.  Formats: E4M3 = 0,
+// E5M2 = 1, E2M3 = 3, E3M2 = 4, E2M1 = 5.  a_sf / b_sf select the byte of the
+// 32-bit Tensor Memory scale words that this K = 32 step uses.
+constexpr uint32_t kMxE4M3 = 0, kMxE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mx_f32(int M, int N, uint32_t afmt, uint32_t bfmt, uint32_t a_sf,
+                                                    uint32_t b_sf) {
+  return (b_sf << 4) | (afmt << 7) | (bfmt << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23)  // scales: UE8M0
+         | ((uint32_t)(M >> 4) << 24) | (a_sf << 29);
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                "r"(ncols)
@@ -73,6 +84,45 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
           d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= (A * 2^(sfa - 127)) * (B * 2^(sfb - 127))^T, one K = 32 step of
+// kind::mxf8f6f4: A and B in shared memory (K-major, 128-byte swizzle, one
+// byte per element: 8-bit types as they are, E2M1 as 16 codes in 8 bytes
+// followed by an 8-byte gap), UE8M0 scales in Tensor Memory.  Scale layout
+// used here: for operand rows 0..127, column c + j of lane 32 q + l holds the
+// 32-bit scale word of row l + 32 j, in each lane quarter q (byte b of a word
+// = the scale of K-block b, picked by the descriptor's a_sf / b_sf).
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// As umma_mx, keeping A in the tensor core's A collector for the next MMA
+// (fill) or taking it from there and releasing it (lastuse): two MMAs that
+// share A read it from shared memory once.
+__device__ __forceinline__ void umma_mx_fill(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X.collector::a::fill [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_mx_lastuse(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X.collector::a::lastuse [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 
@@ -123,12 +173,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+// 32 lanes x 4 columns (see tmem_st32).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+               "r"(v2), "r"(v3)
+               : "memory");
+}
 // Wait until this thread's tcgen05.st writes have completed.
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Asynchronous 16-byte global -> shared copy (generic proxy) and its groups.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Asynchronous 8-byte global -> shared copy (both addresses 8-byte aligned).
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 // As cp_async16, but copies src_bytes (0 or 16) and zero-fills the rest.
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
@@ -159,6 +219,29 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
           smem_u32(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Tensor-map gather of four rows y0..y3 (box: one row of the map's box width
+// at column x) into consecutive rows of shared memory at dst (128-byte
+// aligned; the map's swizzle follows the shared-memory address).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* map, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Make a tensor map that this kernel (or an earlier one) wrote to global
+// memory visible to the tensor-map proxy before its first use here.
+__device__ __forceinline__ void tmap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
+// Prefetch the cache line holding `addr` (global memory) into L2.
+__device__ __forceinline__ void prefetch_l2_line(const void* addr) {
+  asm volatile("prefetch.L2 [%0];" ::"l"(addr));
 }
 
 // Bulk prefetch of global memory into L2 (no data returned to the SM).

@@ -139,3 +139,27 @@ def test_prefill_full_size_sampled(name, tokens):
     inp = synth.make_inputs(synth.WORKLOADS[name])
     _, rel, mx = _forward_check(inp, tokens=tokens)
     print(f"{name}: rel-L2 {rel:.2e}, max-abs/rms {mx:.2e} on tokens {tokens}")
+
+
+def test_prefill_unaligned_codes_flagged_not_read():
+    """The prefill gate/up GEMM reads code matrices with tensor-map copies,
+    which need 32-byte aligned rows: an expert whose gate codes are 16- but not
+    32-byte aligned is flagged (MOE_ERR_DEVICE_CHECK) and its codes are never
+    copied; the next clean call on the same workspace matches the oracle."""
+    wl = synth.Workload("pf_unaligned", 130, 256, 8, 2, 128)
+    inp = synth.make_inputs(wl, seed=8)
+    L = DeviceLayer(inp)
+    good = L.table.desc.clone()
+    bad = good.clone()
+    bad[3, 0] += 16  # gate.q of expert 3: 16-byte aligned, not 32
+    L.table.desc.copy_(bad)
+    L.forward(path=PREFILL)
+    torch().cuda.synchronize()
+    assert L.status() == L.moe.MOE_ERR_DEVICE_CHECK
+    L.table.desc.copy_(good)
+    out, ids, w = L.forward(path=PREFILL)
+    torch().cuda.synchronize()
+    assert L.status() == 0
+    _, same = check_route(inp, ids.cpu().numpy(), w.cpu().numpy())
+    toks = np.nonzero(same)[0]
+    check_out(out.cpu().numpy()[toks], oracle_out(inp, toks), "after unaligned codes")
