@@ -50,7 +50,9 @@ struct Ws {
   uint8_t* xp;          // [2][T*k][H] prefill: each routed pair's activations as two E4M3
                         // terms, rows in bucket order (aliases y)
   int32_t* pinv;        // [T*k] prefill: bucket position of each routed pair (-1: none)
-  void* tmaps;          // [E][2] prefill: tensor maps (128 bytes each) of the gate and up codes
+  void* tmaps;          // [E][3] prefill: tensor maps (128 bytes each) of the gate, up, down codes
+  uint8_t* h8;          // [3][T*k][I] prefill: routed h rows as three E4M3 terms (in y's region,
+                        // after the f16 h rows)
   float* x8scale;       // [T]     2^-tau_t of token t's E4M3 terms
   void* h;              // fp32 h: [T*k][I] (decode) or [T*k + T][I] (prefill; rows
                         // T*k.. hold the shared expert's h)
@@ -65,6 +67,10 @@ struct Ws {
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Tokens per tile of the prefill path's block-scaled gate/up GEMM (two
+// accumulator buffers of gate + up columns fit Tensor Memory).
+constexpr int kPfNTileGu = 112;
 
 // Splits of the contraction of the router GEMM (64 experts x 64 tokens per
 // CTA) for batches above 64 tokens (smaller ones keep their workspace size;
@@ -110,16 +116,17 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
     // all active experts number at most ceil(T*k/128) + min(E, T*k).
     const size_t pairs = T * k;
     const size_t ntiles = (pairs + 127) / 128 + (E < pairs ? E : pairs);
+    const size_t ntiles_gu = (pairs + kPfNTileGu - 1) / kPfNTileGu + (E < pairs ? E : pairs);
     const size_t shtiles = (T + 127) / 128;
     const size_t mgu = (I + 127) / 128, mdn = (H + 127) / 128;
-    ws.items_gu = (int4*)take((ntiles + shtiles) * mgu * 16);
+    ws.items_gu = (int4*)take((ntiles_gu + shtiles) * mgu * 16);
     ws.items_dn = (int4*)take((ntiles + shtiles) * mdn * 16);
   }
   ws.xh = (uint16_t*)take(T * H * 2);
   ws.xscale = (float*)take(T * 4);
   ws.x8scale = (float*)take(T * 4);
   ws.pinv = (int32_t*)take(T * k * 4);
-  ws.tmaps = (void*)take(E * 2 * 128);
+  ws.tmaps = (void*)take(E * 3 * 128);
   // Tokens the decode path may take for this shape (0: it cannot).
   const size_t Td = T <= (size_t)kDecodeBatchMaxT ? T : 0;
   // h in fp32: Td*k rows for the decode path, T*k + T rows for the prefill
@@ -135,12 +142,15 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   // shared expert, after the routed experts' combine has consumed y (and then
   // without the E4M3 rows); on the prefill path the f16 h is written after
   // the gate/up GEMM, the last reader of the E4M3 rows.
-  const size_t y_dec = Td * k * H * 4, h16_pf = hrows * I * 2, xp_pf = 2 * T * k * H;
-  size_t yreg = y_dec > h16_pf ? y_dec : h16_pf;
+  // The E4M3 h terms follow the f16 h rows (both are read by the down GEMMs).
+  const size_t h8_off = align_up(hrows * I * 2, 256);
+  const size_t y_dec = Td * k * H * 4, hy_pf = h8_off + 3 * T * k * I, xp_pf = 2 * T * k * H;
+  size_t yreg = y_dec > hy_pf ? y_dec : hy_pf;
   yreg = yreg > xp_pf ? yreg : xp_pf;
   ws.y = (float*)take(yreg);
   ws.h16 = (uint16_t*)ws.y;
   ws.xp = (uint8_t*)ws.y;
+  ws.h8 = (uint8_t*)ws.y + h8_off;
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
   const size_t S = (size_t)router_splits(s.T, s.E, s.H);
   ws.rpart = (float2*)take(S > 1 ? S * T * E * 8 : 0);
@@ -347,7 +357,8 @@ struct BucketParams {
   const int32_t* ids;      // [T][k]
   int32_t* offsets_out;    // [E+1] caller copy or NULL
   int32_t* sorted_out;     // [T*k] caller copy or NULL
-  int n_tile;              // prefill token tile (columns of one MMA tile)
+  int n_tile;              // prefill token tile (columns of one MMA tile): down GEMM
+  int n_tile_gu;           // prefill token tile of the routed gate/up GEMM
   int m_tiles_gu;          // prefill row tiles of gate/up (ceil(I/128))
   int m_tiles_dn;          // prefill row tiles of down (ceil(H/128))
   Ws ws;

@@ -222,6 +222,68 @@ __global__ void __launch_bounds__(256) k_h_to_f16(ExpertParams p, int row0, int 
   }
 }
 
+// Routed h rows [0, T k) (fp32, bucket order) as three E4M3 terms for the
+// block-scaled down GEMM: with tau_r = 7 - floor(log2 max|h_r|), v = h * 2^tau_r
+// has its largest magnitude in [128, 256); h1 = e4m3(v), h2 = e4m3(16 (v - h1)),
+// h3 = e4m3(16 (16 (v - h1) - h2)), so v = h1 + h2 / 16 + h3 / 256 up to the
+// rounding of h3: 12 significant bits (one more than f16) for every element
+// that stays an E4M3 normal number through the terms, and an absolute error
+// below 2^-18 (2^-25 of the row's maximum) for the others.  hscale[r] =
+// 2^-tau_r.  A row holding an infinity or NaN (its maximum's bits at or above
+// infinity) becomes NaN in every term (E4M3 has no infinity).  One warp per
+// row; I % 128 == 0.
+__device__ __forceinline__ uint32_t e4m3x2_bits(float lo, float hi) {
+  unsigned short q;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(hi), "f"(lo));
+  return q;
+}
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t q) {
+  uint32_t f2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f2) : "h"((unsigned short)q));
+  return __half22float2(*reinterpret_cast<const __half2*>(&f2));
+}
+__global__ void __launch_bounds__(256) k_h_to_e4m3(ExpertParams p) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int n = p.T * p.k, I = p.I;
+  if (row >= n) return;
+  const uint32_t m = p.ws.hmax[row];
+  const int e = (int)((m >> 23) & 0xFFu);
+  const bool bad = e == 0xFF;
+  int tau = (m == 0u || bad) ? 0 : 7 - (e - 127);
+  tau = tau > 126 ? 126 : (tau < -126 ? -126 : tau);
+  const float up = __int_as_float((tau + 127) << 23);
+  if (lane == 0) p.ws.hscale[row] = __int_as_float((127 - tau) << 23);
+  const float* src = reinterpret_cast<const float*>(p.ws.h) + (size_t)row * I;
+  uint8_t* d1 = p.ws.h8 + (size_t)row * I;
+  uint8_t* d2 = d1 + (size_t)n * I;
+  uint8_t* d3 = d2 + (size_t)n * I;
+  for (int c = lane * 4; c < I; c += 128) {
+    uint32_t o1 = 0x7F7F7F7Fu, o2 = 0x7F7F7F7Fu, o3 = 0x7F7F7F7Fu;
+    if (!bad) {
+      const float4 v4 = *reinterpret_cast<const float4*>(src + c);
+      const float v[4] = {v4.x * up, v4.y * up, v4.z * up, v4.w * up};
+      o1 = o2 = o3 = 0u;
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const float a = v[2 * pr], b = v[2 * pr + 1];
+        const uint32_t q1 = e4m3x2_bits(a, b);
+        const float2 f1 = e4m3x2_value(q1);
+        const float ra = (a - f1.x) * 16.f, rb = (b - f1.y) * 16.f;
+        const uint32_t q2 = e4m3x2_bits(ra, rb);
+        const float2 f2 = e4m3x2_value(q2);
+        const uint32_t q3 = e4m3x2_bits((ra - f2.x) * 16.f, (rb - f2.y) * 16.f);
+        o1 |= q1 << (16 * pr);
+        o2 |= q2 << (16 * pr);
+        o3 |= q3 << (16 * pr);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(d1 + c) = o1;
+    *reinterpret_cast<uint32_t*>(d2 + c) = o2;
+    *reinterpret_cast<uint32_t*>(d3 + c) = o3;
+  }
+}
+
 cudaError_t launch_x_to_f16(const ExpertParams& p, cudaStream_t s) {
   k_x_to_f16<<<p.T, 256, 0, s>>>(p);
   return cudaGetLastError();
@@ -260,9 +322,10 @@ __global__ void __launch_bounds__(256) k_shared_sigma(ExpertParams p) {
 }
 
 // ------------------------------------------------------------ work items --
-// Items are (expert, 128-row weight tile, 128-token tile).  Routed items come
+// Items are (expert, 128-row weight tile, token tile).  Routed items come
 // first, active experts in ascending order, row tiles outer; then the shared
-// expert's items when there is one.
+// expert's items when there is one.  Token tiles hold up to 128 tokens, the
+// routed gate/up items (block-scaled GEMM) up to kPfNTileGu.
 struct PfItem {
   int shared;  // 1: the bf16 shared expert
   int e;       // routed expert
@@ -277,19 +340,19 @@ struct PfItem {
 // items [pref[u], pref[u+1]) in row-tile-major order, then the shared
 // expert's items.  One warp per active expert.
 __device__ __forceinline__ void pf_fill_items(const ExpertParams& p, const int32_t* pref, int4* items, int M, int u,
-                                              int U) {
+                                              int U, int ntile) {
   const int lane = threadIdx.x & 31;
   const int m_tiles = (M + kPfMTile - 1) / kPfMTile;
   if (u < U) {
     const int e = p.ws.act_e[u];
     const int b0 = p.offsets[e];
     const int n = p.offsets[e + 1] - b0;
-    const int ntiles = (n + kPfNTile - 1) / kPfNTile;
+    const int ntiles = (n + ntile - 1) / ntile;
     const int base = pref[u];
     const int count = ntiles * m_tiles;
     for (int local = lane; local < count; local += 32) {
       const int m = local / ntiles, nt = local - m * ntiles;
-      items[base + local] = make_int4(e, m * kPfMTile, b0 + nt * kPfNTile, min(kPfNTile, n - nt * kPfNTile));
+      items[base + local] = make_int4(e, m * kPfMTile, b0 + nt * ntile, min(ntile, n - nt * ntile));
     }
   } else if (p.sh_gate) {
     const int base = U > 0 ? pref[U] : 0;
@@ -306,9 +369,9 @@ __global__ void __launch_bounds__(256) k_pf_items(ExpertParams p) {
   const int nwarps = (int)(gridDim.x * blockDim.x) >> 5;
   for (int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); w <= 2 * U + 1; w += nwarps) {
     if (w <= U)
-      pf_fill_items(p, p.ws.act_pref_gu, p.ws.items_gu, p.I, w, U);
+      pf_fill_items(p, p.ws.act_pref_gu, p.ws.items_gu, p.I, w, U, kPfNTileGu);
     else
-      pf_fill_items(p, p.ws.act_pref_dn, p.ws.items_dn, p.H, w - U - 1, U);
+      pf_fill_items(p, p.ws.act_pref_dn, p.ws.items_dn, p.H, w - U - 1, U, kPfNTile);
   }
 }
 
@@ -1016,56 +1079,79 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const
   }
 }
 
-// --------------------------------------------- block-scaled gate/up GEMM --
+// ------------------------------------------------ block-scaled expert GEMMs --
 // The tensor core takes the MXFP4 weights as they are stored: tcgen05.mma
 // kind::mxf8f6f4 with A = E2M1 codes and their E8M0 block scales, and B = the
-// activations as two E4M3 terms (k_x_to_e4m3, rows in bucket order), scale
-// 2^0 for x1 and 2^-4 for x2.  Products are exact and accumulate in fp32 in Tensor Memory; nothing is
-// converted on CUDA cores and no operand passes through registers.  Work items
-// are those of k_pf_gemm (routed experts only); per 128-element slice of the
-// contraction (four MX blocks):
-//   * one producer thread loads the 128 gate and 128 up code rows with one
-//     tensor-map copy each (4-bit elements in the 16-codes-then-8-byte-gap
-//     layout the MMA reads, 128-byte swizzle; per-expert maps written by
-//     k_pf_mx_maps) and the item's token rows of both E4M3 terms, which are
-//     contiguous in bucket order, in boxes of 32 rows;
+// activations as E4M3 terms in bucket order: for gate/up the token rows as two
+// terms (k_x_to_e4m3, x * 2^tau = x1 + x2 / 16, exact for bf16), for down the
+// h rows as three (k_h_to_e4m3, h * 2^tau ~ h1 + h2 / 16 + h3 / 256, 12
+// significant bits).  The terms enter with constant block scales 2^0, 2^-4,
+// 2^-8.  Products are exact and accumulate in fp32 in Tensor Memory; nothing
+// is converted on CUDA cores and no operand passes through registers.  Work
+// items are those of k_pf_gemm (routed experts only).  Per 128-element slice
+// of the contraction (four MX blocks):
+//   * one producer thread loads the 128 weight rows of each matrix with one
+//     tensor-map copy (4-bit elements in the 16-codes-then-8-byte-gap layout
+//     the MMA reads, 128-byte swizzle; per-expert maps written by
+//     k_pf_mx_maps) and the item's activation rows of all terms, contiguous
+//     in bucket order, as one box of rows x terms (the box height is the token
+//     count rounded up to 32: one of four maps);
 //   * 4 scale warps (one per TMEM lane quarter) write the rows' scale words
 //     (4 bytes = the slice's four blocks) into the stage's scale columns;
-//   * one thread issues 16 MMAs (4 K-steps x gate/up x 2 terms, M = 128,
-//     N = round16(tokens), K = 32; the two terms share one read of A through
-//     the A collector) and releases the stage with tcgen05.commit;
-//   * 4 epilogue warps apply SwiGLU with the token's 2^-tau and store h in
-//     fp32 as k_pf_gemm does (with the h-row maxima for the f16 pass).
+//   * one thread issues the MMAs (4 K-steps x matrices x terms, M = 128,
+//     N = round16(tokens), K = 32; the terms share one read of A through the
+//     A collector) and releases the stage with tcgen05.commit;
+//   * 4 epilogue warps read one of two accumulator buffers while the MMAs fill
+//     the other: gate/up apply SwiGLU with the token's 2^-tau and store h in
+//     fp32 (with each h row's largest |h|); down adds w * 2^-tau * y into out
+//     with fp32 atomics.
 // Code matrices must be 32-byte aligned for their tensor maps (checked: an
-// expert whose gate or up codes are not is flagged and skipped).
+// expert whose codes are not is flagged and skipped).
 namespace mxk {
 constexpr int kSliceK = 128;
 constexpr int kStages = 3;
 constexpr int kTile = 128 * 128;                // one 128-row operand tile (bytes)
-constexpr int kStageBytes = 4 * kTile;           // gate codes, up codes, x1, x2
+constexpr int kStageBytes = 4 * kTile;           // weight tiles + activation box
 constexpr int kCodeTx = 128 * 64;                // bytes a code tile's copy delivers (4-bit codes)
-constexpr int kXBox = 32;                        // token rows per activation copy
+constexpr int kXBox = 32;                        // granule of the activation box heights
+constexpr int kXMaps = 4;                        // box heights 32, 64, 96, 128
 constexpr int kTmaWarp = 1;                      // warp 0: MMA issuer, owns TMEM
 constexpr int kSfWarp0 = 2, kSfWarps = 4;        // warps 2-5
 constexpr int kEpWarp0 = kSfWarp0 + kSfWarps, kEpWarps = 4;  // warps 6-9
 constexpr int kThreads = (kEpWarp0 + kEpWarps) * 32;
-// TMEM columns: gate accumulator [0, 128), up [128, 256); activation-term
-// scales [256, 260) = 2^0 and [260, 264) = 2^-4; weight scales of stage st,
-// matrix a at 264 + 8 st + 4 a.
-constexpr uint32_t kColSfb = 256, kColSfa = 264;
 constexpr uint32_t kTmemCols = 512;
-static_assert(kColSfa + 8 * kStages <= kTmemCols, "TMEM columns");
 constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
 }  // namespace mxk
+
+// TMEM columns: two accumulator buffers of AccW columns (matrix a at a * N of
+// the buffer); the terms' constant scales (4 columns each) at ColSfb; the
+// weight scales of stage st, matrix a at ColSfa + 4 (NA st + a).
+template <bool GU>
+struct MxCfg {
+  static constexpr int NA = GU ? 2 : 1;                   // weight matrices per item
+  static constexpr int NT = GU ? 2 : 3;                   // activation terms
+  static constexpr int N = GU ? kPfNTileGu : kPfNTile;    // tokens per tile (at most)
+  static constexpr uint32_t AccW = NA * N;
+  static constexpr uint32_t ColSfb = 2 * AccW;
+  static constexpr uint32_t ColSfa = ColSfb + 4 * NT;
+  static_assert(ColSfa + 4 * NA * mxk::kStages <= mxk::kTmemCols, "TMEM columns");
+  static_assert(NA * mxk::kTile + NT * mxk::kXMaps * mxk::kXBox * 128 <= mxk::kStageBytes, "stage bytes");
+};
 
 struct MxShared {
   uint64_t full[mxk::kStages];   // stage filled: producer (with the copies' bytes) + 4 scale warps
   uint64_t empty[mxk::kStages];  // stage consumed: tcgen05.commit
-  uint64_t accf;                 // accumulators ready: tcgen05.commit
-  uint64_t acce;                 // accumulators drained: 4 epilogue warps
+  uint64_t accf[2];              // accumulator buffer ready: tcgen05.commit
+  uint64_t acce[2];              // accumulator buffer drained: 4 epilogue warps
   uint32_t tmem_base;
   int abort_flag;
-  float col_scale[mxk::kEpWarps][kPfNTile];  // per epilogue warp: 2^-tau of each column's token
+  float col_scale[mxk::kEpWarps][kPfNTile];  // per epilogue warp: factor of each column
+  int col_tok[mxk::kEpWarps][kPfNTile];      // per epilogue warp: token of each column (down)
+};
+
+// Maps of the bucket-order activation rows of all terms, one per box height.
+struct MxXMaps {
+  CUtensorMap m[mxk::kXMaps];
 };
 
 struct MxCtx {
@@ -1073,7 +1159,8 @@ struct MxCtx {
   uint8_t* ring;  // kStages x kStageBytes, 1024-byte aligned
   int n_items;
   const int4* items;
-  int ns;  // slices per item
+  int ns;         // slices per item
+  int srow;       // scale bytes per weight row (K / 32)
   WsHeader* hdr;
   long long wait_limit;
 };
@@ -1105,44 +1192,54 @@ __device__ __forceinline__ bool mx_claim(const MxCtx& c, int gs, uint32_t backof
   return mx_warp_wait(c, &c.sh->empty[st], (use - 1) & 1, backoff_ns);
 }
 
-// Gate and up code matrices usable by the tensor-map copies.
+// Code matrices of one GEMM usable by the tensor-map copies.
+template <bool GU>
 __device__ __forceinline__ bool mx_codes_ok(const moe_expert& ex) {
-  return expert_ptrs_ok(ex) && (((uintptr_t)ex.gate.q | (uintptr_t)ex.up.q) & 31u) == 0;
+  const uintptr_t q = GU ? ((uintptr_t)ex.gate.q | (uintptr_t)ex.up.q) : (uintptr_t)ex.down.q;
+  return expert_ptrs_ok(ex) && (q & 31u) == 0;
+}
+// Scale matrix a of an expert in one GEMM.
+template <bool GU>
+__device__ __forceinline__ const uint8_t* mx_scales(const moe_expert& ex, int a) {
+  return GU ? (a == 0 ? ex.gate.s : ex.up.s) : ex.down.s;
 }
 
-// Tensor maps of the active experts' gate and up codes: the template (dims
-// H x I, row stride H / 2 bytes, box 128 x 128, 4-bit elements with 8-byte
-// gaps, 128-byte swizzle) with the expert's address.  Experts whose codes
-// cannot be mapped are flagged (MOE_ERR_DEVICE_CHECK) and get no map; the
-// GEMM skips their copies.  One thread per (active expert, matrix).
-__global__ void k_pf_mx_maps(ExpertParams p, const __grid_constant__ CUtensorMap tmpl) {
+// Tensor maps of the active experts' codes, [E][3] (gate, up, down): the
+// templates (gate/up: dims H x I, row stride H / 2 bytes; down: I x H, I / 2;
+// boxes of 128 elements x 128 rows, 4-bit elements with 8-byte gaps, 128-byte
+// swizzle) with the expert's address.  Experts whose codes cannot be mapped
+// are flagged (MOE_ERR_DEVICE_CHECK) and get no map; the GEMMs skip their
+// copies.  One thread per (active expert, matrix).
+__global__ void k_pf_mx_maps(ExpertParams p, const __grid_constant__ CUtensorMap tmpl_gu,
+                             const __grid_constant__ CUtensorMap tmpl_dn) {
   const int U = (int)p.ws.hdr->n_active;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * U; i += gridDim.x * blockDim.x) {
-    const int e = __ldg(&p.ws.act_e[i >> 1]);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 3 * U; i += gridDim.x * blockDim.x) {
+    const int e = __ldg(&p.ws.act_e[i / 3]), a = i % 3;
     const moe_expert ex = p.experts[e];
-    if (!mx_codes_ok(ex)) {
-      if ((i & 1) == 0) set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
+    const uint8_t* q = a == 0 ? ex.gate.q : (a == 1 ? ex.up.q : ex.down.q);
+    if (!expert_ptrs_ok(ex) || ((uintptr_t)q & 31u) != 0) {
+      set_status(p.ws.hdr, MOE_ERR_DEVICE_CHECK);
       continue;
     }
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ws.tmaps) + (size_t)(2 * e + (i & 1)) * 128);
-    const uint4* src = reinterpret_cast<const uint4*>(&tmpl);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ws.tmaps) + (size_t)(3 * e + a) * 128);
+    const uint4* src = reinterpret_cast<const uint4*>(a < 2 ? &tmpl_gu : &tmpl_dn);
 #pragma unroll
     for (int j = 0; j < 8; ++j) dst[j] = src[j];
-    const uint8_t* q = (i & 1) ? ex.up.q : ex.gate.q;
     asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(q) : "memory");
     asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
   }
 }
 
 // Producer warp.  Per slice: claim the stage; lane 0 arms the stage's barrier
-// with the bytes of all copies and issues the two code-tile copies and the
-// token-row boxes of both terms (rows past the item's tokens belong to the
-// next bucket or read as zero: they only feed accumulator columns that the
-// epilogue ignores).  Its lane issues nothing else: the copy unit's queue is
-// what the tensor core waits on.
-__device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const CUtensorMap* xmap) {
+// with the bytes of all copies and issues the code-tile copies and the
+// activation box (rows past the item's tokens belong to the next bucket or
+// read as zero: they only feed accumulator columns that the epilogue
+// ignores).  Its lane issues nothing else: the copy unit's queue is what the
+// tensor core waits on.
+template <bool GU>
+__device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const MxXMaps* xmaps) {
+  using C = MxCfg<GU>;
   const int lane = threadIdx.x & 31;
-  const int npairs = p.T * p.k;
   MxShared& sh = *c.sh;
   int gs = 0;
   bool ok = true;
@@ -1152,14 +1249,15 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const CU
   for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x) {
     const PfItem it = pf_item(item, p, c.items);
     const moe_expert ex = p.experts[it.e];
-    const bool wok = mx_codes_ok(ex);
-    const int nbox = (it.cnt + mxk::kXBox - 1) / mxk::kXBox;
-    const uint8_t* maps = reinterpret_cast<const uint8_t*>(p.ws.tmaps) + (size_t)2 * it.e * 128;
-    if (wok && lane == 0) {
-      tmap_acquire(maps);
-      tmap_acquire(maps + 128);
-    }
-    const uint32_t tx = (wok ? 2u * mxk::kCodeTx : 0u) + 2u * (uint32_t)nbox * mxk::kXBox * mxk::kSliceK;
+    const bool wok = mx_codes_ok<GU>(ex);
+    const int nbox = (it.cnt + mxk::kXBox - 1) / mxk::kXBox;  // box height / 32
+    const CUtensorMap* xmap = &xmaps->m[nbox - 1];
+    const uint8_t* maps = reinterpret_cast<const uint8_t*>(p.ws.tmaps) + (size_t)(3 * it.e + (GU ? 0 : 2)) * 128;
+    if (wok && lane == 0)
+#pragma unroll
+      for (int a = 0; a < C::NA; ++a) tmap_acquire(maps + a * 128);
+    const uint32_t tx =
+        (wok ? (uint32_t)C::NA * mxk::kCodeTx : 0u) + (uint32_t)(C::NT * nbox * mxk::kXBox) * mxk::kSliceK;
     for (int s = 0; s < c.ns; ++s, ++gs) {
       if (!mx_claim(c, gs, mxk::kPollTma)) {
         ok = false;
@@ -1170,15 +1268,11 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const CU
         uint8_t* sb = c.ring + (size_t)st * mxk::kStageBytes;
         uint64_t* bar = &sh.full[st];
         mbar_arrive_expect_tx(bar, tx);
-        if (wok) {
-          tma_load_2d(sb, maps, s * mxk::kSliceK, it.m0, bar);
-          tma_load_2d(sb + mxk::kTile, maps + 128, s * mxk::kSliceK, it.m0, bar);
-        }
-        for (int b = 0; b < nbox; ++b) {
-          const int y = it.p0 + b * mxk::kXBox;
-          tma_load_2d(sb + 2 * mxk::kTile + b * mxk::kXBox * 128, xmap, s * mxk::kSliceK, y, bar);
-          tma_load_2d(sb + 3 * mxk::kTile + b * mxk::kXBox * 128, xmap, s * mxk::kSliceK, npairs + y, bar);
-        }
+        if (wok)
+#pragma unroll
+          for (int a = 0; a < C::NA; ++a)
+            tma_load_2d(sb + a * mxk::kTile, maps + a * 128, s * mxk::kSliceK, it.m0, bar);
+        tma_load_3d(sb + C::NA * mxk::kTile, xmap, s * mxk::kSliceK, it.hpos0, 0, bar);
 #pragma unroll
         for (int i = 0; i < mxk::kStages; ++i)
           if (i == st) issued[i] = gs / mxk::kStages;
@@ -1195,54 +1289,62 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const CU
       if (issued[i] >= 0 && !mbar_wait(&sh.full[i], issued[i] & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
 }
 
-// Scale warps: warp quarter q writes, in lanes 32q..32q+31, the activation
-// terms' constant scales once, then per slice the scale words of gate and up
-// rows lane + 32 j (j = 0..3) into the stage's columns (the same words in
-// every quarter).  An expert that is skipped gets scale 1 (its rows are
-// discarded by the epilogue).  A slice reads 4 bytes of each scale row, so
-// the words are loaded kSfAhead slices ahead into a register ring, and the
-// rows are prefetched into L2 when an item starts (and the next item's
-// halfway through).
+// Scale warps: warp quarter q writes, in lanes 32q..32q+31, the terms'
+// constant scales once, then per slice the scale words of rows lane + 32 j
+// (j = 0..3) of each matrix into the stage's columns (the same words in every
+// quarter).  An expert that is skipped gets scale 1 (its rows are discarded by
+// the epilogue).  A slice reads 4 bytes of each scale row, so the words are
+// loaded kSfAhead slices ahead into a register ring, and the rows are
+// prefetched into L2 when an item starts (and the next item's halfway
+// through).
 constexpr int kSfAhead = 4;
+template <bool GU>
 __device__ __forceinline__ void mx_prefetch_scale_rows(const ExpertParams& p, const MxCtx& c, int item, int r) {
+  using C = MxCfg<GU>;
   if (item >= c.n_items) return;
   const PfItem it = pf_item(item, p, c.items);
   const moe_expert ex = p.experts[it.e];
-  if (!mx_codes_ok(ex)) return;
-  const size_t srow = (size_t)p.H / 32;
-  const uint8_t* rows[2] = {ex.gate.s + (size_t)(it.m0 + r) * srow, ex.up.s + (size_t)(it.m0 + r) * srow};
+  if (!mx_codes_ok<GU>(ex)) return;
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
-    for (size_t o = 0; o < srow; o += 128) prefetch_l2_line(rows[a] + o);
-#pragma unroll
-  for (int a = 0; a < 2; ++a) prefetch_l2_line(rows[a] + srow - 1);
+  for (int a = 0; a < C::NA; ++a) {
+    const uint8_t* row = mx_scales<GU>(ex, a) + (size_t)(it.m0 + r) * c.srow;
+    for (int o = 0; o < c.srow; o += 128) prefetch_l2_line(row + o);
+    prefetch_l2_line(row + c.srow - 1);
+  }
 }
 
+template <bool GU>
 __device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+  using C = MxCfg<GU>;
+  constexpr int NW = 4 * C::NA;  // scale words a lane writes per slice
   const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const uint32_t lbase = tmem + ((uint32_t)(q * 32) << 16);
-  tmem_st4(lbase + mxk::kColSfb, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-  tmem_st4(lbase + mxk::kColSfb + 4, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
-  const size_t srow = (size_t)p.H / 32;  // scale bytes per row (a multiple of 4)
-  const size_t jstride = 32 * srow / 4;  // words between rows lane and lane + 32
+#pragma unroll
+  for (int j = 0; j < C::NT; ++j) {
+    const uint32_t v = (uint32_t)(127 - 4 * j) * 0x01010101u;  // 2^(-4 j)
+    tmem_st4(lbase + C::ColSfb + 4 * j, v, v, v, v);
+  }
+  const size_t jstride = 32 * (size_t)c.srow / 4;  // words between rows lane and lane + 32
   int gs = 0;
   bool ok = true;
-  mx_prefetch_scale_rows(p, c, blockIdx.x, q * 32 + lane);
+  mx_prefetch_scale_rows<GU>(p, c, blockIdx.x, q * 32 + lane);
   for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x) {
     const PfItem it = pf_item(item, p, c.items);
     const moe_expert ex = p.experts[it.e];
-    const bool wok = mx_codes_ok(ex);
-    const uint32_t* sg = wok ? reinterpret_cast<const uint32_t*>(ex.gate.s + (size_t)(it.m0 + lane) * srow) : nullptr;
-    const uint32_t* su = wok ? reinterpret_cast<const uint32_t*>(ex.up.s + (size_t)(it.m0 + lane) * srow) : nullptr;
-    // Words of slice sl: w[0..3] gate rows lane + 32 j, w[4..7] up rows.
-    auto load = [&](uint32_t (&w)[8], int sl) {
+    const bool wok = mx_codes_ok<GU>(ex);
+    const uint32_t* sp[C::NA];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        w[j] = (wok && sl < c.ns) ? __ldg(sg + j * jstride + sl) : 0x7F7F7F7Fu;
-        w[4 + j] = (wok && sl < c.ns) ? __ldg(su + j * jstride + sl) : 0x7F7F7F7Fu;
-      }
+    for (int a = 0; a < C::NA; ++a)
+      sp[a] = wok ? reinterpret_cast<const uint32_t*>(mx_scales<GU>(ex, a) + (size_t)(it.m0 + lane) * c.srow)
+                  : nullptr;
+    // Words of slice sl: w[4 a + j] = row lane + 32 j of matrix a.
+    auto load = [&](uint32_t (&w)[NW], int sl) {
+#pragma unroll
+      for (int a = 0; a < C::NA; ++a)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[4 * a + j] = (wok && sl < c.ns) ? __ldg(sp[a] + j * jstride + sl) : 0x7F7F7F7Fu;
     };
-    uint32_t ring[kSfAhead][8];
+    uint32_t ring[kSfAhead][NW];
 #pragma unroll
     for (int i = 0; i < kSfAhead; ++i) load(ring[i], i);
     for (int s0 = 0; s0 < c.ns && ok; s0 += kSfAhead) {
@@ -1250,15 +1352,17 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tm
       for (int i = 0; i < kSfAhead; ++i) {
         const int s = s0 + i;
         if (s >= c.ns) break;
-        if (s == c.ns / 2) mx_prefetch_scale_rows(p, c, item + gridDim.x, q * 32 + lane);
+        if (s == c.ns / 2) mx_prefetch_scale_rows<GU>(p, c, item + gridDim.x, q * 32 + lane);
         if (!mx_claim(c, gs, mxk::kPollSf)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int st = gs % mxk::kStages;
-        tmem_st4(lbase + mxk::kColSfa + 8 * st, ring[i][0], ring[i][1], ring[i][2], ring[i][3]);
-        tmem_st4(lbase + mxk::kColSfa + 8 * st + 4, ring[i][4], ring[i][5], ring[i][6], ring[i][7]);
+#pragma unroll
+        for (int a = 0; a < C::NA; ++a)
+          tmem_st4(lbase + C::ColSfa + 4 * (C::NA * st + a), ring[i][4 * a], ring[i][4 * a + 1], ring[i][4 * a + 2],
+                   ring[i][4 * a + 3]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -1272,19 +1376,25 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tm
   tmem_st_wait();
 }
 
-// MMA issuer (lane 0 of warp 0): per item, wait for the accumulators to be
-// drained, then per slice for the stage, issue the 16 MMAs and commit the
-// stage; after the last slice commit the accumulators.  The operands were
-// written by tensor-map copies (async proxy), so no proxy fence is needed.
+// MMA issuer (lane 0 of warp 0): per item, wait for its accumulator buffer
+// (item parity) to be drained, then per slice for the stage, issue the MMAs
+// and commit the stage; after the last slice commit the buffer.  The operands
+// were written by tensor-map copies (async proxy), so no proxy fence is
+// needed.
+template <bool GU>
 __device__ void mx_mma_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+  using C = MxCfg<GU>;
   MxShared& sh = *c.sh;
   int ci = 0, gs = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.items);
-    if (ci >= 1 && !mx_wait(c, &sh.acce, (ci - 1) & 1, mxk::kPollMma)) break;
+    const int b = ci & 1, use = ci >> 1;
+    if (use >= 1 && !mx_wait(c, &sh.acce[b], (use - 1) & 1, mxk::kPollMma)) break;
     tc_fence_after();
     const int nmma = (it.cnt + 15) & ~15;
     const uint32_t ibase = idesc_mx_f32(kPfMTile, nmma, kMxE2M1, kMxE4M3, 0, 0);
+    // Term j's rows start j box heights x 128 bytes into the activation box.
+    const uint32_t xstep = (uint32_t)((it.cnt + mxk::kXBox - 1) / mxk::kXBox) * mxk::kXBox * 128;
     bool ok = true;
     for (int s = 0; s < c.ns; ++s, ++gs) {
       const int st = gs % mxk::kStages;
@@ -1294,104 +1404,137 @@ __device__ void mx_mma_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem
       }
       tc_fence_after();
       const uint32_t sbase = smem_u32(c.ring + (size_t)st * mxk::kStageBytes);
+      const uint32_t xbase = sbase + C::NA * mxk::kTile;
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
         const uint32_t idesc = ibase | ((uint32_t)kb << 29) | ((uint32_t)kb << 4);
-        const uint64_t b1 = sdesc_sw128(sbase + 2 * mxk::kTile + 32 * kb);
-        const uint64_t b2 = sdesc_sw128(sbase + 3 * mxk::kTile + 32 * kb);
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < C::NA; ++a) {
           const uint64_t ad = sdesc_sw128(sbase + a * mxk::kTile + 32 * kb);
-          const uint32_t d = tmem + (uint32_t)(a * 128);
-          const uint32_t sfa = tmem + mxk::kColSfa + (uint32_t)(8 * st + 4 * a);
-          umma_mx_fill(d, ad, b1, idesc, sfa, tmem + mxk::kColSfb, (s > 0 || kb > 0) ? 1u : 0u);
-          umma_mx_lastuse(d, ad, b2, idesc, sfa, tmem + mxk::kColSfb + 4, 1u);
+          const uint32_t d = tmem + (uint32_t)b * C::AccW + (uint32_t)(a * C::N);
+          const uint32_t sfa = tmem + C::ColSfa + (uint32_t)(4 * (C::NA * st + a));
+#pragma unroll
+          for (int j = 0; j < C::NT; ++j) {
+            const uint64_t bd = sdesc_sw128(xbase + j * xstep + 32 * kb);
+            const uint32_t sfb = tmem + C::ColSfb + 4u * j;
+            if (j == 0)
+              umma_mx_fill(d, ad, bd, idesc, sfa, sfb, (s > 0 || kb > 0) ? 1u : 0u);
+            else if (j < C::NT - 1)
+              umma_mx_use(d, ad, bd, idesc, sfa, sfb, 1u);
+            else
+              umma_mx_lastuse(d, ad, bd, idesc, sfa, sfb, 1u);
+          }
         }
       }
       umma_commit(&sh.empty[st]);
     }
-    umma_commit(&sh.accf);
+    umma_commit(&sh.accf[b]);
     if (!ok) {
       ++ci;
       break;
     }
   }
   // Every MMA issued must have finished before TMEM is released.
-  if (ci > 0 && !mbar_wait(&sh.accf, (ci - 1) & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
+  if (ci > 0 && !mbar_wait(&sh.accf[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
 }
 
 // Epilogue warps: warp q reads TMEM lanes 32q..32q+31 (weight rows m0 + 32q +
-// lane): h[hpos0 + n][row] = silu(g) * u with both scaled by the token's
-// 2^-tau, in fp32, raising each h row's largest |h| into hmax.  A row with a
-// NaN block scale (E8M0 code 255) in gate or up gives NaN, as the definition
+// lane).
+//   gate/up: h[hpos0 + n][row] = silu(g) * u with both scaled by the token's
+//            2^-tau, in fp32, raising each h row's largest |h| into hmax;
+//   down:    out[token(n)][row] += w(n) * 2^-tau(n) * y.
+// A row with a NaN block scale (E8M0 code 255) gives NaN, as the definition
 // of the format has it (checked here, while the item's MMAs run).
+template <bool GU>
 __device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+  using C = MxCfg<GU>;
   MxShared& sh = *c.sh;
   const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int npairs = p.T * p.k;
-  const int nsw = p.H / 128;  // scale words per row
+  const int nsw = c.srow / 4;  // scale words per row
   float* hout = reinterpret_cast<float*>(p.ws.h);
   int ci = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.items);
     const int row = it.m0 + q * 32 + lane;
     const moe_expert ex = p.experts[it.e];
-    const bool valid = mx_codes_ok(ex);
+    const bool valid = mx_codes_ok<GU>(ex);
     bool nan_row = false;
     if (valid) {
-      const uint32_t* g = reinterpret_cast<const uint32_t*>(ex.gate.s + (size_t)row * (p.H / 32));
-      const uint32_t* u = reinterpret_cast<const uint32_t*>(ex.up.s + (size_t)row * (p.H / 32));
       uint32_t any = 0u;
+#pragma unroll
+      for (int a = 0; a < C::NA; ++a) {
+        const uint32_t* sr = reinterpret_cast<const uint32_t*>(mx_scales<GU>(ex, a) + (size_t)row * c.srow);
 #pragma unroll 8
-      for (int i = 0; i < nsw; ++i) {
-        const uint32_t a = __ldg(g + i), b = __ldg(u + i);
-        // A byte equal to 0xFF: all of its bits set (per-byte test without carries).
-        any |= (a & (a >> 1) & (a >> 2) & (a >> 3) & (a >> 4) & (a >> 5) & (a >> 6) & (a >> 7)) & 0x01010101u;
-        any |= (b & (b >> 1) & (b >> 2) & (b >> 3) & (b >> 4) & (b >> 5) & (b >> 6) & (b >> 7)) & 0x01010101u;
+        for (int i = 0; i < nsw; ++i) {
+          const uint32_t w = __ldg(sr + i);
+          // A byte equal to 0xFF: all of its bits set (per-byte test without carries).
+          any |= (w & (w >> 1) & (w >> 2) & (w >> 3) & (w >> 4) & (w >> 5) & (w >> 6) & (w >> 7)) & 0x01010101u;
+        }
       }
       nan_row = any != 0u;
     }
     float* col_scale = sh.col_scale[q];
+    int* col_tok = sh.col_tok[q];
     __syncwarp();
     for (int n = lane; n < it.cnt; n += 32) {
       int pr = __ldg(&p.sorted[it.p0 + n]);
-      if (pr < 0 || pr >= npairs) pr = 0;  // flagged by the producer
-      col_scale[n] = __ldg(&p.ws.x8scale[pr / p.k]);
+      if (pr < 0 || pr >= npairs) pr = 0;  // flagged when the list was checked
+      const int t = pr / p.k;
+      col_tok[n] = t;
+      col_scale[n] = GU ? __ldg(&p.ws.x8scale[t]) : __ldg(&p.w[pr]) * __ldg(&p.ws.hscale[it.hpos0 + n]);
     }
     __syncwarp();
-    if (!mx_warp_wait(c, &sh.accf, ci & 1, mxk::kPollEp)) break;
+    const int b = ci & 1;
+    if (!mx_warp_wait(c, &sh.accf[b], (ci >> 1) & 1, mxk::kPollEp)) break;
     tc_fence_after();
-    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * C::AccW;
     for (int c0 = 0; c0 < it.cnt; c0 += 16) {
-      uint32_t g[16], u[16];
+      uint32_t g[16];
       tmem_ld16(tbase + (uint32_t)c0, g);
-      tmem_ld16(tbase + 128u + (uint32_t)c0, u);
-      tmem_ld_wait();
-      uint32_t habs = 0u;
+      if (GU) {
+        uint32_t u[16];
+        tmem_ld16(tbase + (uint32_t)C::N + (uint32_t)c0, u);
+        tmem_ld_wait();
+        uint32_t habs = 0u;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int n = c0 + i;
-        uint32_t av = 0u;
-        if (valid && n < it.cnt) {
-          const float xs = col_scale[n];
-          float hv = silu_f32(__uint_as_float(g[i]) * xs) * (__uint_as_float(u[i]) * xs);
-          if (nan_row) hv = __int_as_float(0x7FC00000);
-          hout[(size_t)(it.hpos0 + n) * p.I + row] = hv;
-          av = __float_as_uint(hv) & 0x7FFFFFFFu;
+        for (int i = 0; i < 16; ++i) {
+          const int n = c0 + i;
+          uint32_t av = 0u;
+          if (valid && n < it.cnt) {
+            const float xs = col_scale[n];
+            float hv = silu_f32(__uint_as_float(g[i]) * xs) * (__uint_as_float(u[i]) * xs);
+            if (nan_row) hv = __int_as_float(0x7FC00000);
+            hout[(size_t)(it.hpos0 + n) * p.I + row] = hv;
+            av = __float_as_uint(hv) & 0x7FFFFFFFu;
+          }
+          const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, av);
+          if (lane == i) habs = mx;
         }
-        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, av);
-        if (lane == i) habs = mx;
+        if (lane < 16 && c0 + lane < it.cnt && habs != 0u) atomicMax(&p.ws.hmax[it.hpos0 + c0 + lane], habs);
+      } else {
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = c0 + i;
+            if (n < it.cnt) {
+              float v = __uint_as_float(g[i]) * col_scale[n];
+              if (nan_row) v = __int_as_float(0x7FC00000);
+              atomicAdd(&p.out[(size_t)col_tok[n] * p.H + row], v);
+            }
+          }
+        }
       }
-      if (lane < 16 && c0 + lane < it.cnt && habs != 0u) atomicMax(&p.ws.hmax[it.hpos0 + c0 + lane], habs);
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.acce);
+    if (lane == 0) mbar_arrive(&sh.acce[b]);
   }
 }
 
-__global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx_gateup(ExpertParams p,
-                                                                   const __grid_constant__ CUtensorMap xmap) {
+template <bool GU>
+__global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, const __grid_constant__ MxXMaps xmaps) {
   extern __shared__ uint8_t mx_dyn[];
   __shared__ MxShared sh;
   const int warp = threadIdx.x >> 5;
@@ -1404,8 +1547,10 @@ __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx_gateup(ExpertParams 
       mbar_init(&sh.full[s], 1 + mxk::kSfWarps);
       mbar_init(&sh.empty[s], 1);
     }
-    mbar_init(&sh.accf, 1);
-    mbar_init(&sh.acce, mxk::kEpWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.accf[b], 1);
+      mbar_init(&sh.acce[b], mxk::kEpWarps);
+    }
     sh.abort_flag = 0;
     mbar_init_fence();
   }
@@ -1417,19 +1562,21 @@ __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx_gateup(ExpertParams 
   c.sh = &sh;
   c.ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mx_dyn) + 1023) & ~(uintptr_t)1023);
   const int U = (int)p.ws.hdr->n_active;
-  c.n_items = U > 0 ? __ldg(&p.ws.act_pref_gu[U]) : 0;
-  c.items = p.ws.items_gu;
-  c.ns = p.H / mxk::kSliceK;
+  c.n_items = U > 0 ? __ldg(&(GU ? p.ws.act_pref_gu : p.ws.act_pref_dn)[U]) : 0;
+  c.items = GU ? p.ws.items_gu : p.ws.items_dn;
+  const int K = GU ? p.H : p.I;
+  c.ns = K / mxk::kSliceK;
+  c.srow = K / 32;
   c.hdr = p.ws.hdr;
   c.wait_limit = p.wait_limit;
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) mx_mma_role(p, c, tmem);
+    if ((threadIdx.x & 31) == 0) mx_mma_role<GU>(p, c, tmem);
   } else if (warp == mxk::kTmaWarp) {
-    mx_producer_role(p, c, &xmap);
+    mx_producer_role<GU>(p, c, &xmaps);
   } else if (warp < mxk::kEpWarp0) {
-    mx_scale_role(p, c, tmem);
+    mx_scale_role<GU>(p, c, tmem);
   } else {
-    mx_epilogue_role(p, c, tmem);
+    mx_epilogue_role<GU>(p, c, tmem);
   }
   tc_fence_before();
   __syncthreads();
@@ -1477,16 +1624,16 @@ cudaError_t encode_h16_map(CUtensorMap* m, void* base, int rows, int I) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-// Template of the per-expert code maps of the block-scaled gate/up GEMM: an
-// [I][H] matrix of 4-bit codes (row stride H / 2 bytes), boxes of 128
-// elements x 128 rows, each 16 codes stored as 8 bytes followed by an 8-byte
-// gap, 128-byte swizzle.  `base` only has to be a valid 32-byte-aligned
-// address: k_pf_mx_maps replaces it per expert.
-cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int H, int I) {
+// Template of the per-expert code maps of the block-scaled GEMMs: an [M][K]
+// matrix of 4-bit codes (row stride K / 2 bytes), boxes of 128 elements x 128
+// rows, each 16 codes stored as 8 bytes followed by an 8-byte gap, 128-byte
+// swizzle.  `base` only has to be a valid 32-byte-aligned address:
+// k_pf_mx_maps replaces it per expert.
+cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int K, int M) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)I};
-  const cuuint64_t strides[1] = {(cuuint64_t)H / 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
   const cuuint32_t box[2] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)kPfMTile};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
@@ -1495,17 +1642,18 @@ cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int H, int I) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Map of the bucket-order E4M3 activation rows of both terms as one
-// [2 T k][H] byte matrix: boxes of 32 rows x 128 bytes, 128-byte swizzle;
-// rows past the end read as zero.
-cudaError_t encode_xp_map(CUtensorMap* m, void* base, int npairs, int H) {
+// Map of bucket-order E4M3 activation rows as a [terms][T k][K] byte tensor
+// (term, row, byte): boxes of 128 bytes x `rows` rows x all terms, 128-byte
+// swizzle, the terms' rows one after the other in shared memory; rows past
+// the end read as zero.
+cudaError_t encode_terms_map(CUtensorMap* m, void* base, int npairs, int K, int terms, int rows) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)2 * npairs};
-  const cuuint64_t strides[1] = {(cuuint64_t)H};
-  const cuuint32_t box[2] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)mxk::kXBox};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+  const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)npairs, (cuuint64_t)terms};
+  const cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)npairs * K};
+  const cuuint32_t box[3] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)rows, (cuuint32_t)terms};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -1522,16 +1670,17 @@ constexpr size_t pf_smem_bytes() {
 cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   if (!p.x_bf16 || !prefill_supported(p.H, p.I)) return cudaErrorNotSupported;
   const int nsm = device_sm_count();
+  const int npairs = p.T * p.k;
   cudaError_t err;
   // Bucket layout, active experts and tile prefixes come from the routing or
   // bucketing kernels already on the stream.  Routed experts run on the
-  // block-scaled gate/up GEMM (E4M3 activation terms); the bf16 shared expert
-  // on k_pf_gemm (f16 activations).
+  // block-scaled GEMMs (E4M3 activation terms); the bf16 shared expert on
+  // k_pf_gemm (f16 operands).
   const bool routed = !p.shared_only;
   if (routed) {
     // Bucket position of every routed pair, then the pairs' E4M3 rows.
-    if ((err = cudaMemsetAsync(p.ws.pinv, 0xFF, (size_t)p.T * p.k * 4, s)) != cudaSuccess) return err;
-    k_pf_pinv<<<(p.T * p.k + 255) / 256, 256, 0, s>>>(p);
+    if ((err = cudaMemsetAsync(p.ws.pinv, 0xFF, (size_t)npairs * 4, s)) != cudaSuccess) return err;
+    k_pf_pinv<<<(npairs + 255) / 256, 256, 0, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     k_x_to_e4m3<<<p.T, 256, 0, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -1552,42 +1701,58 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   constexpr size_t dn_smem = pf_smem_bytes<false>();
   static_assert(gu_smem + sizeof(PfShared) <= 227 * 1024 && dn_smem + sizeof(PfShared) <= 227 * 1024, "smem");
   static_assert(mx_smem + sizeof(MxShared) <= 227 * 1024, "smem");
-  if ((err = ensure_smem_attr((const void*)k_pf_mx_gateup, mx_smem)) != cudaSuccess) return err;
+  if ((err = ensure_smem_attr((const void*)k_pf_mx<true>, mx_smem)) != cudaSuccess) return err;
+  if ((err = ensure_smem_attr((const void*)k_pf_mx<false>, mx_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
-  CUtensorMap tmap_h, tmap_codes, tmap_xp;
+  CUtensorMap tmap_h, tmpl_gu, tmpl_dn;
+  MxXMaps xmaps, hmaps;
   memset(&tmap_h, 0, sizeof tmap_h);
-  memset(&tmap_codes, 0, sizeof tmap_codes);
-  memset(&tmap_xp, 0, sizeof tmap_xp);
-  if ((err = encode_h16_map(&tmap_h, p.ws.h16, p.T * p.k + p.T, p.I)) != cudaSuccess) return err;
+  memset(&tmpl_gu, 0, sizeof tmpl_gu);
+  memset(&tmpl_dn, 0, sizeof tmpl_dn);
+  memset(&xmaps, 0, sizeof xmaps);
+  memset(&hmaps, 0, sizeof hmaps);
+  if ((err = encode_h16_map(&tmap_h, p.ws.h16, npairs + p.T, p.I)) != cudaSuccess) return err;
   if (routed) {
-    if ((err = encode_code_map_template(&tmap_codes, p.ws.tmaps, p.H, p.I)) != cudaSuccess) return err;
-    if ((err = encode_xp_map(&tmap_xp, p.ws.xp, p.T * p.k, p.H)) != cudaSuccess) return err;
-    k_pf_mx_maps<<<(2 * p.E + 255) / 256, 256, 0, s>>>(p, tmap_codes);
+    if ((err = encode_code_map_template(&tmpl_gu, p.ws.tmaps, p.H, p.I)) != cudaSuccess) return err;
+    if ((err = encode_code_map_template(&tmpl_dn, p.ws.tmaps, p.I, p.H)) != cudaSuccess) return err;
+    for (int i = 0; i < mxk::kXMaps; ++i) {
+      const int rows = (i + 1) * mxk::kXBox;
+      if ((err = encode_terms_map(&xmaps.m[i], p.ws.xp, npairs, p.H, MxCfg<true>::NT, rows)) != cudaSuccess ||
+          (err = encode_terms_map(&hmaps.m[i], p.ws.h8, npairs, p.I, MxCfg<false>::NT, rows)) != cudaSuccess)
+        return err;
+    }
+    k_pf_mx_maps<<<(3 * p.E + 255) / 256, 256, 0, s>>>(p, tmpl_gu, tmpl_dn);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
+  ExpertParams ps = p;  // the shared expert's items alone
+  ps.shared_only = 1;
   prof_before(MOE_STAGE_PF_GATEUP, s);
-  if (routed) k_pf_mx_gateup<<<nsm, mxk::kThreads, mx_smem, s>>>(p, tmap_xp);
+  if (routed) k_pf_mx<true><<<nsm, mxk::kThreads, mx_smem, s>>>(p, xmaps);
   if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
-    ExpertParams ps = p;
-    ps.shared_only = 1;
     k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(ps, tmap_h);
     err = cudaGetLastError();
   }
   prof_after(MOE_STAGE_PF_GATEUP, s);
   if (err != cudaSuccess) return err;
-  // f16 h rows for the down GEMM: the routed pairs' rows (none when the
-  // shared expert runs alone) and the shared expert's.
-  const int hrow0 = p.shared_only ? p.T * p.k : 0;
-  const int hrow1 = p.T * p.k + (p.sh_gate ? p.T : 0);
-  if (hrow1 > hrow0) {
-    k_h_to_f16<<<(hrow1 - hrow0 + 7) / 8, 256, 0, s>>>(p, hrow0, hrow1);
+  // Down operands: the routed pairs' h rows as E4M3 terms, the shared
+  // expert's as f16.
+  if (routed) {
+    k_h_to_e4m3<<<(npairs + 7) / 8, 256, 0, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  if (p.sh_gate) {
+    k_h_to_f16<<<(p.T + 7) / 8, 256, 0, s>>>(p, npairs, npairs + p.T);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   prof_before(MOE_STAGE_PF_DOWN, s);
-  k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(p, tmap_h);
+  if (routed) k_pf_mx<false><<<nsm, mxk::kThreads, mx_smem, s>>>(p, hmaps);
+  if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
+    k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(ps, tmap_h);
+    err = cudaGetLastError();
+  }
   prof_after(MOE_STAGE_PF_DOWN, s);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace moe

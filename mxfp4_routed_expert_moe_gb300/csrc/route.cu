@@ -20,19 +20,20 @@ namespace moe {
 // ws.offsets (and the caller's copy), plus the active-expert list and the
 // prefill tile prefixes.  Called by every thread of one CTA.
 __device__ void plan_scan(const BucketParams& p) {
-  __shared__ int warp_tot[3][32];
-  __shared__ int carry[3];
+  __shared__ int warp_tot[4][32];
+  __shared__ int carry[4];
   const int E = p.E, tid = threadIdx.x, nthreads = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nw = nthreads >> 5;
-  if (tid < 3) carry[tid] = 0;
+  if (tid < 4) carry[tid] = 0;
   __syncthreads();
   for (int base = 0; base < E; base += nthreads) {
     const int e = base + tid;
     const int c = e < E ? __ldcg(&p.ws.offsets[e]) : 0;
-    int v[3] = {c, c > 0 ? 1 : 0, c > 0 ? (c + p.n_tile - 1) / p.n_tile : 0};
-    int incl[3];
+    int v[4] = {c, c > 0 ? 1 : 0, c > 0 ? (c + p.n_tile - 1) / p.n_tile : 0,
+                c > 0 ? (c + p.n_tile_gu - 1) / p.n_tile_gu : 0};
+    int incl[4];
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < 4; ++q) {
       incl[q] = v[q];
 #pragma unroll
       for (int m = 1; m < 32; m <<= 1) {
@@ -42,9 +43,9 @@ __device__ void plan_scan(const BucketParams& p) {
       if (lane == 31) warp_tot[q][warp] = incl[q];
     }
     __syncthreads();
-    int excl[3];
+    int excl[4];
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < 4; ++q) {
       int pre = carry[q];
       for (int w = 0; w < warp; ++w) pre += warp_tot[q][w];
       excl[q] = pre + incl[q] - v[q];
@@ -55,13 +56,13 @@ __device__ void plan_scan(const BucketParams& p) {
       if (p.offsets_out) p.offsets_out[e] = excl[0];
       if (c > 0) {
         p.ws.act_e[excl[1]] = e;
-        p.ws.act_pref_gu[excl[1]] = excl[2] * p.m_tiles_gu;
+        p.ws.act_pref_gu[excl[1]] = excl[3] * p.m_tiles_gu;
         p.ws.act_pref_dn[excl[1]] = excl[2] * p.m_tiles_dn;
       }
     }
     if (tid == 0) {
 #pragma unroll
-      for (int q = 0; q < 3; ++q)
+      for (int q = 0; q < 4; ++q)
         for (int w = 0; w < nw; ++w) carry[q] += warp_tot[q][w];
     }
     __syncthreads();
@@ -70,7 +71,7 @@ __device__ void plan_scan(const BucketParams& p) {
     p.ws.offsets[E] = carry[0];
     if (p.offsets_out) p.offsets_out[E] = carry[0];
     p.ws.hdr->n_active = (uint32_t)carry[1];
-    p.ws.act_pref_gu[carry[1]] = carry[2] * p.m_tiles_gu;
+    p.ws.act_pref_gu[carry[1]] = carry[3] * p.m_tiles_gu;
     p.ws.act_pref_dn[carry[1]] = carry[2] * p.m_tiles_dn;
   }
 }
