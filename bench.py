@@ -594,7 +594,7 @@ def reference_arm(args, rank, world):
 
 
 # -------------------------------------------------------------------- sweep --
-SWEEP_T = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)
+SWEEP_T = (1, 2, 4, 8, 16, 32, 48, 64, 96, 128, 192, 256, 384, 512, 768, 1024)
 
 
 def sweep(args, device):

@@ -121,7 +121,8 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
  *            MOE_DECODE_BATCH_MAX_T; else prefill.  A bf16 shape that the
  *            decode kernels do not take (H > 8192) goes to prefill when that
  *            path takes it.  The bound is the measured crossover of the two
- *            paths on GB300: below it the decode path's single pass over the
+ *            paths on GB300 (T near 265 at H = 7168, E = 896, k = 16,
+ *            I = 1408): below it the decode path's single pass over the
  *            active experts' weights is faster than the tensor-core GEMMs,
  *            whose per-tile cost needs many tokens per expert. */
 typedef enum {
@@ -132,7 +133,7 @@ typedef enum {
 
 #define MOE_DECODE_MAX_T 64
 #define MOE_DECODE_BATCH_MAX_T 1024
-#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 10
+#define MOE_DECODE_AUTO_PAIRS_PER_EXPERT 5
 
 typedef struct { const uint8_t* q; const uint8_t* s; } moe_mx_mat;   /* see above */
 typedef struct { moe_mx_mat gate, up, down; } moe_expert;            /* six tensors */

@@ -32,7 +32,7 @@ PATH_DECODE = 1
 PATH_PREFILL = 2
 DECODE_MAX_T = 64                  # MOE_DECODE_MAX_T
 DECODE_BATCH_MAX_T = 1024          # MOE_DECODE_BATCH_MAX_T
-DECODE_AUTO_PAIRS_PER_EXPERT = 10  # MOE_DECODE_AUTO_PAIRS_PER_EXPERT
+DECODE_AUTO_PAIRS_PER_EXPERT = 5  # MOE_DECODE_AUTO_PAIRS_PER_EXPERT
 
 # Every symbol the header declares (checked by the tests against the .so).
 EXPORTS = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_route", "moe_mxfp4_experts",

@@ -145,7 +145,8 @@ def test_select_path_rules(moe):
     # A shared expert does not change the choice: the decode path runs it on
     # the prefill kernels after the routed experts (bf16, H and I % 128 == 0).
     assert sel(1, H, E, I, k, shared=True) == D
-    assert sel(512, H, E, I, k, shared=True) == D
+    assert sel(t_max, H, E, I, k, shared=True) == D
+    assert sel(512, H, E, I, k, shared=True) == P
     assert sel(4096, H, E, I, k, shared=True) == P
     with pytest.raises(moe.MoeError) as ei:
         sel(1, 7168 + 32, E, I, k, shared=True)
