@@ -1109,9 +1109,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const
 // expert whose codes are not is flagged and skipped).
 namespace mxk {
 constexpr int kSliceK = 128;
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;
 constexpr int kTile = 128 * 128;                // one 128-row operand tile (bytes)
-constexpr int kStageBytes = 4 * kTile;           // weight tiles + activation box
 constexpr int kCodeTx = 128 * 64;                // bytes a code tile's copy delivers (4-bit codes)
 constexpr int kXBox = 32;                        // granule of the activation box heights
 constexpr int kXMaps = 4;                        // box heights 32, 64, 96, 128
@@ -1123,30 +1122,38 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
 }  // namespace mxk
 
-// TMEM columns: two accumulator buffers of AccW columns (matrix a at a * N of
-// the buffer); the terms' constant scales (4 columns each) at ColSfb; the
-// weight scales of stage st, matrix a at ColSfa + 4 (NA st + a).
+// Per GEMM: a stage holds the NA weight tiles and an activation box of up to
+// N rows (rounded up to 32) of each of the NT terms: 64 KB, three stages
+// (gate/up: N = 112; down: N = 128).  A fourth stage with 96-token gate/up
+// tiles was slower: more items outweighed the deeper ring.  TMEM columns: two
+// accumulator buffers of AccW columns (matrix a at a * N of the buffer); the
+// terms' constant scales (4 columns each) at ColSfb; the weight scales of
+// stage st, matrix a at ColSfa + 4 (NA st + a).
 template <bool GU>
 struct MxCfg {
   static constexpr int NA = GU ? 2 : 1;                   // weight matrices per item
   static constexpr int NT = GU ? 2 : 3;                   // activation terms
   static constexpr int N = GU ? kPfNTileGu : kPfNTile;    // tokens per tile (at most)
+  static constexpr int XROWS = (N + mxk::kXBox - 1) / mxk::kXBox * mxk::kXBox;
+  static constexpr int STAGE = NA * mxk::kTile + NT * XROWS * 128;
+  static constexpr int STAGES = 3;
   static constexpr uint32_t AccW = NA * N;
   static constexpr uint32_t ColSfb = 2 * AccW;
   static constexpr uint32_t ColSfa = ColSfb + 4 * NT;
-  static_assert(ColSfa + 4 * NA * mxk::kStages <= mxk::kTmemCols, "TMEM columns");
-  static_assert(NA * mxk::kTile + NT * mxk::kXMaps * mxk::kXBox * 128 <= mxk::kStageBytes, "stage bytes");
+  static_assert(ColSfa + 4 * NA * STAGES <= mxk::kTmemCols, "TMEM columns");
+  static_assert(STAGES <= mxk::kMaxStages && STAGE % 1024 == 0, "stages");
 };
 
+template <bool GU>
 struct MxShared {
-  uint64_t full[mxk::kStages];   // stage filled: producer (with the copies' bytes) + 4 scale warps
-  uint64_t empty[mxk::kStages];  // stage consumed: tcgen05.commit
-  uint64_t accf[2];              // accumulator buffer ready: tcgen05.commit
-  uint64_t acce[2];              // accumulator buffer drained: 4 epilogue warps
+  uint64_t full[mxk::kMaxStages];   // stage filled: producer (with the copies' bytes) + 4 scale warps
+  uint64_t empty[mxk::kMaxStages];  // stage consumed: tcgen05.commit
+  uint64_t accf[2];                 // accumulator buffer ready: tcgen05.commit
+  uint64_t acce[2];                 // accumulator buffer drained: 4 epilogue warps
   uint32_t tmem_base;
   int abort_flag;
-  float col_scale[mxk::kEpWarps][kPfNTile];  // per epilogue warp: factor of each column
-  int col_tok[mxk::kEpWarps][kPfNTile];      // per epilogue warp: token of each column (down)
+  float col_scale[mxk::kEpWarps][MxCfg<GU>::N];       // per epilogue warp: factor of each column
+  int col_tok[mxk::kEpWarps][GU ? 1 : MxCfg<GU>::N];  // per epilogue warp: token of each column (down)
 };
 
 // Maps of the bucket-order activation rows of all terms, one per box height.
@@ -1154,9 +1161,10 @@ struct MxXMaps {
   CUtensorMap m[mxk::kXMaps];
 };
 
+template <bool GU>
 struct MxCtx {
-  MxShared* sh;
-  uint8_t* ring;  // kStages x kStageBytes, 1024-byte aligned
+  MxShared<GU>* sh;
+  uint8_t* ring;  // STAGES x STAGE bytes, 1024-byte aligned
   int n_items;
   const int4* items;
   int ns;         // slices per item
@@ -1165,8 +1173,9 @@ struct MxCtx {
   long long wait_limit;
 };
 
-__device__ __forceinline__ bool mx_wait(const MxCtx& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
-  MxShared& sh = *c.sh;
+template <bool GU>
+__device__ __forceinline__ bool mx_wait(const MxCtx<GU>& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
+  MxShared<GU>& sh = *c.sh;
   const bool diag = c.wait_limit < kWaitCycles;
   if (diag ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
@@ -1181,13 +1190,16 @@ __device__ __forceinline__ bool mx_wait(const MxCtx& c, uint64_t* bar, uint32_t 
     }
   }
 }
-__device__ __forceinline__ bool mx_warp_wait(const MxCtx& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
+template <bool GU>
+__device__ __forceinline__ bool mx_warp_wait(const MxCtx<GU>& c, uint64_t* bar, uint32_t parity, uint32_t backoff_ns) {
   const bool ok = mx_wait(c, bar, parity, backoff_ns);
   return __all_sync(0xFFFFFFFFu, ok);
 }
-// Wait until ring stage gs % kStages is free for global slice gs.
-__device__ __forceinline__ bool mx_claim(const MxCtx& c, int gs, uint32_t backoff_ns) {
-  const int st = gs % mxk::kStages, use = gs / mxk::kStages;
+// Wait until ring stage gs % STAGES is free for global slice gs.
+template <bool GU>
+__device__ __forceinline__ bool mx_claim(const MxCtx<GU>& c, int gs, uint32_t backoff_ns) {
+  constexpr int S = MxCfg<GU>::STAGES;
+  const int st = gs % S, use = gs / S;
   if (use == 0) return true;
   return mx_warp_wait(c, &c.sh->empty[st], (use - 1) & 1, backoff_ns);
 }
@@ -1230,6 +1242,7 @@ __global__ void k_pf_mx_maps(ExpertParams p, const __grid_constant__ CUtensorMap
   }
 }
 
+constexpr int kMxAhead = 4;
 // Producer warp.  Per slice: claim the stage; lane 0 arms the stage's barrier
 // with the bytes of all copies and issues the code-tile copies and the
 // activation box (rows past the item's tokens belong to the next bucket or
@@ -1237,15 +1250,16 @@ __global__ void k_pf_mx_maps(ExpertParams p, const __grid_constant__ CUtensorMap
 // ignores).  Its lane issues nothing else: the copy unit's queue is what the
 // tensor core waits on.
 template <bool GU>
-__device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const MxXMaps* xmaps) {
+__device__ void mx_producer_role(const ExpertParams& p, const MxCtx<GU>& c, const MxXMaps* xmaps) {
   using C = MxCfg<GU>;
   const int lane = threadIdx.x & 31;
-  MxShared& sh = *c.sh;
+  MxShared<GU>& sh = *c.sh;
   int gs = 0;
   bool ok = true;
-  int issued[mxk::kStages];  // last use of each stage with copies issued (-1: none)
+  constexpr int S = C::STAGES;
+  int issued[S];  // last use of each stage with copies issued (-1: none)
 #pragma unroll
-  for (int i = 0; i < mxk::kStages; ++i) issued[i] = -1;
+  for (int i = 0; i < S; ++i) issued[i] = -1;
   for (int item = blockIdx.x; item < c.n_items && ok; item += gridDim.x) {
     const PfItem it = pf_item(item, p, c.items);
     const moe_expert ex = p.experts[it.e];
@@ -1264,8 +1278,8 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const Mx
         break;
       }
       if (lane == 0) {
-        const int st = gs % mxk::kStages;
-        uint8_t* sb = c.ring + (size_t)st * mxk::kStageBytes;
+        const int st = gs % S;
+        uint8_t* sb = c.ring + (size_t)st * C::STAGE;
         uint64_t* bar = &sh.full[st];
         mbar_arrive_expect_tx(bar, tx);
         if (wok)
@@ -1273,9 +1287,13 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const Mx
           for (int a = 0; a < C::NA; ++a)
             tma_load_2d(sb + a * mxk::kTile, maps + a * 128, s * mxk::kSliceK, it.m0, bar);
         tma_load_3d(sb + C::NA * mxk::kTile, xmap, s * mxk::kSliceK, it.hpos0, 0, bar);
+        // The code boxes kMxAhead slices on into L2 (they come from DRAM).
+        if (wok && s + kMxAhead < c.ns)
 #pragma unroll
-        for (int i = 0; i < mxk::kStages; ++i)
-          if (i == st) issued[i] = gs / mxk::kStages;
+          for (int a = 0; a < C::NA; ++a) tma_prefetch_2d(maps + a * 128, (s + kMxAhead) * mxk::kSliceK, it.m0);
+#pragma unroll
+        for (int i = 0; i < S; ++i)
+          if (i == st) issued[i] = gs / S;
       }
       __syncwarp();
     }
@@ -1285,7 +1303,7 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const Mx
   // normal run: the MMA issuer waited for each of them).
   if (lane == 0)
 #pragma unroll
-    for (int i = 0; i < mxk::kStages; ++i)
+    for (int i = 0; i < S; ++i)
       if (issued[i] >= 0 && !mbar_wait(&sh.full[i], issued[i] & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
 }
 
@@ -1299,7 +1317,7 @@ __device__ void mx_producer_role(const ExpertParams& p, const MxCtx& c, const Mx
 // through).
 constexpr int kSfAhead = 4;
 template <bool GU>
-__device__ __forceinline__ void mx_prefetch_scale_rows(const ExpertParams& p, const MxCtx& c, int item, int r) {
+__device__ __forceinline__ void mx_prefetch_scale_rows(const ExpertParams& p, const MxCtx<GU>& c, int item, int r) {
   using C = MxCfg<GU>;
   if (item >= c.n_items) return;
   const PfItem it = pf_item(item, p, c.items);
@@ -1314,7 +1332,7 @@ __device__ __forceinline__ void mx_prefetch_scale_rows(const ExpertParams& p, co
 }
 
 template <bool GU>
-__device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+__device__ void mx_scale_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem) {
   using C = MxCfg<GU>;
   constexpr int NW = 4 * C::NA;  // scale words a lane writes per slice
   const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
@@ -1358,7 +1376,7 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tm
           break;
         }
         tc_fence_after();
-        const int st = gs % mxk::kStages;
+        const int st = gs % C::STAGES;
 #pragma unroll
         for (int a = 0; a < C::NA; ++a)
           tmem_st4(lbase + C::ColSfa + 4 * (C::NA * st + a), ring[i][4 * a], ring[i][4 * a + 1], ring[i][4 * a + 2],
@@ -1382,9 +1400,9 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx& c, uint32_t tm
 // were written by tensor-map copies (async proxy), so no proxy fence is
 // needed.
 template <bool GU>
-__device__ void mx_mma_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+__device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem) {
   using C = MxCfg<GU>;
-  MxShared& sh = *c.sh;
+  MxShared<GU>& sh = *c.sh;
   int ci = 0, gs = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.items);
@@ -1397,13 +1415,13 @@ __device__ void mx_mma_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem
     const uint32_t xstep = (uint32_t)((it.cnt + mxk::kXBox - 1) / mxk::kXBox) * mxk::kXBox * 128;
     bool ok = true;
     for (int s = 0; s < c.ns; ++s, ++gs) {
-      const int st = gs % mxk::kStages;
-      if (!mx_wait(c, &sh.full[st], (gs / mxk::kStages) & 1, mxk::kPollMma)) {
+      const int st = gs % C::STAGES;
+      if (!mx_wait(c, &sh.full[st], (gs / C::STAGES) & 1, mxk::kPollMma)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sbase = smem_u32(c.ring + (size_t)st * mxk::kStageBytes);
+      const uint32_t sbase = smem_u32(c.ring + (size_t)st * C::STAGE);
       const uint32_t xbase = sbase + C::NA * mxk::kTile;
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
@@ -1446,9 +1464,9 @@ __device__ void mx_mma_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem
 // A row with a NaN block scale (E8M0 code 255) gives NaN, as the definition
 // of the format has it (checked here, while the item's MMAs run).
 template <bool GU>
-__device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx& c, uint32_t tmem) {
+__device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem) {
   using C = MxCfg<GU>;
-  MxShared& sh = *c.sh;
+  MxShared<GU>& sh = *c.sh;
   const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int npairs = p.T * p.k;
   const int nsw = c.srow / 4;  // scale words per row
@@ -1481,8 +1499,12 @@ __device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx& c, uint32_t
       int pr = __ldg(&p.sorted[it.p0 + n]);
       if (pr < 0 || pr >= npairs) pr = 0;  // flagged when the list was checked
       const int t = pr / p.k;
-      col_tok[n] = t;
-      col_scale[n] = GU ? __ldg(&p.ws.x8scale[t]) : __ldg(&p.w[pr]) * __ldg(&p.ws.hscale[it.hpos0 + n]);
+      if (GU) {
+        col_scale[n] = __ldg(&p.ws.x8scale[t]);
+      } else {
+        col_tok[n] = t;
+        col_scale[n] = __ldg(&p.w[pr]) * __ldg(&p.ws.hscale[it.hpos0 + n]);
+      }
     }
     __syncwarp();
     const int b = ci & 1;
@@ -1535,15 +1557,16 @@ __device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx& c, uint32_t
 
 template <bool GU>
 __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, const __grid_constant__ MxXMaps xmaps) {
+  using C = MxCfg<GU>;
   extern __shared__ uint8_t mx_dyn[];
-  __shared__ MxShared sh;
+  __shared__ MxShared<GU> sh;
   const int warp = threadIdx.x >> 5;
   if (warp == 0) {
     tmem_alloc(&sh.tmem_base, mxk::kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < mxk::kStages; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sh.full[s], 1 + mxk::kSfWarps);
       mbar_init(&sh.empty[s], 1);
     }
@@ -1558,7 +1581,7 @@ __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-  MxCtx c;
+  MxCtx<GU> c;
   c.sh = &sh;
   c.ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mx_dyn) + 1023) & ~(uintptr_t)1023);
   const int U = (int)p.ws.hdr->n_active;
@@ -1696,13 +1719,15 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   }
   k_pf_items<<<nsm, 256, 0, s>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  constexpr size_t mx_smem = (size_t)mxk::kStages * mxk::kStageBytes + 1024;
+  constexpr size_t mxgu_smem = (size_t)MxCfg<true>::STAGES * MxCfg<true>::STAGE + 1024;
+  constexpr size_t mxdn_smem = (size_t)MxCfg<false>::STAGES * MxCfg<false>::STAGE + 1024;
   constexpr size_t gu_smem = pf_smem_bytes<true>();
   constexpr size_t dn_smem = pf_smem_bytes<false>();
   static_assert(gu_smem + sizeof(PfShared) <= 227 * 1024 && dn_smem + sizeof(PfShared) <= 227 * 1024, "smem");
-  static_assert(mx_smem + sizeof(MxShared) <= 227 * 1024, "smem");
-  if ((err = ensure_smem_attr((const void*)k_pf_mx<true>, mx_smem)) != cudaSuccess) return err;
-  if ((err = ensure_smem_attr((const void*)k_pf_mx<false>, mx_smem)) != cudaSuccess) return err;
+  static_assert(mxgu_smem + sizeof(MxShared<true>) <= 227 * 1024, "smem");
+  static_assert(mxdn_smem + sizeof(MxShared<false>) <= 227 * 1024, "smem");
+  if ((err = ensure_smem_attr((const void*)k_pf_mx<true>, mxgu_smem)) != cudaSuccess) return err;
+  if ((err = ensure_smem_attr((const void*)k_pf_mx<false>, mxdn_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<true>, gu_smem)) != cudaSuccess) return err;
   if ((err = ensure_smem_attr((const void*)k_pf_gemm<false>, dn_smem)) != cudaSuccess) return err;
   CUtensorMap tmap_h, tmpl_gu, tmpl_dn;
@@ -1728,7 +1753,7 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   ExpertParams ps = p;  // the shared expert's items alone
   ps.shared_only = 1;
   prof_before(MOE_STAGE_PF_GATEUP, s);
-  if (routed) k_pf_mx<true><<<nsm, mxk::kThreads, mx_smem, s>>>(p, xmaps);
+  if (routed) k_pf_mx<true><<<nsm, mxk::kThreads, mxgu_smem, s>>>(p, xmaps);
   if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
     k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(ps, tmap_h);
     err = cudaGetLastError();
@@ -1746,7 +1771,7 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   prof_before(MOE_STAGE_PF_DOWN, s);
-  if (routed) k_pf_mx<false><<<nsm, mxk::kThreads, mx_smem, s>>>(p, hmaps);
+  if (routed) k_pf_mx<false><<<nsm, mxk::kThreads, mxdn_smem, s>>>(p, hmaps);
   if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
     k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(ps, tmap_h);
     err = cudaGetLastError();

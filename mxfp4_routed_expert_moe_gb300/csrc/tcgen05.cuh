@@ -239,6 +239,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// Prefetch one 2-D box of a tensor map into L2 (no data returned).
+__device__ __forceinline__ void tma_prefetch_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
+}
+
 // Tensor-map gather of four rows y0..y3 (box: one row of the map's box width
 // at column x) into consecutive rows of shared memory at dst (128-byte
 // aligned; the map's swizzle follows the shared-memory address).
