@@ -215,8 +215,9 @@ class Layer:
         return moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, dt, self.shared is not None, self.path) == moe.PATH_DECODE
 
     def launches_per_step(self) -> int:
-        # prefill: router GEMM, top-k, bucket count, bucket scatter, x->fp16, (shared-expert row
-        # shifts), item tables, gate/up, h->fp16, down
+        # prefill: router GEMM, top-k, bucket count, bucket scatter, pair positions, x->E4M3 rows,
+        # item tables, code maps, block-scaled gate/up, h->E4M3, block-scaled down; the shared
+        # expert adds x->fp16, its row shifts, its gate/up, h->fp16 and its down
         if self.decode_path:
             # shared expert: x->fp16, its row shifts, item tables, and the two prefill GEMMs (with
             # the h->fp16 pass between them) on its tiles alone
@@ -225,7 +226,7 @@ class Layer:
                 return 3 + sh  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
             # router GEMM (+ split reduction), top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
             return 8 + sh + (1 if self._router_splits() > 1 else 0)
-        return 9 + (1 if self.shared is not None else 0) + (1 if self._router_splits() > 1 else 0)
+        return 11 + (5 if self.shared is not None else 0) + (1 if self._router_splits() > 1 else 0)
 
     def _router_splits(self) -> int:
         """Splits of the router GEMM's contraction (the library's rule)."""
@@ -381,6 +382,8 @@ def time_e2e(layer, steps, warmup, graph):
     torch.cuda.synchronize()
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
+
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rates of GB300 (4.5 / 2.25 PFLOP/s)
 
 KERNEL_SOURCES = {
     "dec_gateup": ("common.cuh", "async.cuh", "route_small.cuh", "decode.cu"),
@@ -711,14 +714,21 @@ def measure(layer, args, rank, world, local, device, steps, cpu_seconds, parity_
                 "traffic": traffic, "kernel": "k_dec_gateup (MXFP4 gate/up GEMV + SwiGLU)",
                 "bytes_per_launch": gu_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
     else:
+        # The gate/up MMAs are tcgen05 kind::mxf8f6f4 (E2M1 weights x E4M3 activation terms), an
+        # 8-bit-class contraction: its peak is the measured bf16 rate times the nominal fp8 / bf16
+        # ratio (4.5 / 2.25).  Each algorithmic product takes two MMA products (the activation's
+        # two E4M3 terms), so the MMA rate executed is twice `achieved`.
         fl = layer.flops_gateup()
         achieved = fl / (st_ms / 1000.0) / 1e12
+        fp8 = bf16 * FP8_OVER_BF16
         traffic, sha = traffic_from_profiles("pf_gateup", wl.name)
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
-                "traffic": traffic, "kernel": "k_pf_gemm<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
-                "flops_per_launch": fl, "launch_ms": st_ms,
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8, "unit": "TFLOP/s", "frac": achieved / fp8,
+                "traffic": traffic, "kernel": "k_pf_mx<gate/up> (tcgen05 block-scaled grouped GEMM + SwiGLU)",
+                "flops_per_launch": fl, "launch_ms": st_ms, "mma_terms": 2,
+                "frac_of_bf16_peak": achieved / bf16,
                 "hbm_frac_of_step": layer.algorithmic_bytes_step(n_active) / (ms / 1000.0) / 1e9 / hbm,
-                "peak_source": f"{peak_src} (bf16_tflops, burst; f16 operands run at the bf16 rate)"}
+                "peak_source": f"{peak_src} (bf16_tflops burst x {FP8_OVER_BF16:g}, the nominal fp8 / bf16 ratio: "
+                               "the MMAs are kind::mxf8f6f4)"}
     step_bytes = layer.algorithmic_bytes_step(n_active)
     step_flops = layer.flops_step()
     fields = {
