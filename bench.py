@@ -224,9 +224,18 @@ class Layer:
             sh = 6 if self.shared is not None else 0
             if self.wl.T <= self.moe.DECODE_MAX_T:
                 return 3 + sh  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
-            # router GEMM (+ split reduction), top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
-            return 8 + sh + (1 if self._router_splits() > 1 else 0)
-        return 11 + (5 if self.shared is not None else 0) + (1 if self._router_splits() > 1 else 0)
+            # router, top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
+            return 7 + self._router_launches() + sh
+        return 10 + self._router_launches() + (5 if self.shared is not None else 0)
+
+    def _router_launches(self) -> int:
+        """Router kernels of a batch above 64 tokens: the tensor-core screen (W split, screen
+        GEMM, exact candidate scores) for bf16 x, H % 64 == 0 and E <= 4096; else the CUDA-core
+        GEMM (and its split reduction)."""
+        wl = self.wl
+        if wl.x_dtype != "f32" and wl.H % 64 == 0 and wl.E <= 4096:
+            return 3
+        return 1 + (1 if self._router_splits() > 1 else 0)
 
     def _router_splits(self) -> int:
         """Splits of the router GEMM's contraction (the library's rule)."""

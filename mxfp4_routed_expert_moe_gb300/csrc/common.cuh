@@ -62,6 +62,9 @@ struct Ws {
   int32_t* shsig;       // [2I + H] row shifts of the bf16 shared expert (gate, up, down)
   float* y;             // [T*k][H] fp32 (decode, T <= 1024)
   float2* rpart;        // [S][T][E] router partial sums of the S K-splits (S > 1 only)
+  uint16_t* wr16;       // [2][E][H] router weights as two bf16 terms (T > 64 only)
+  float* wrnorm;        // [E] Euclidean norm of each router row, rounded up (T > 64 only)
+  float* sapprox;       // [T][E] tensor-core approximation of the router scores (T > 64 only)
   uint32_t* rowdone;    // [ceil(H/32)] per-row-tile completion counters
   size_t total;
 };
@@ -154,6 +157,10 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
   const size_t S = (size_t)router_splits(s.T, s.E, s.H);
   ws.rpart = (float2*)take(S > 1 ? S * T * E * 8 : 0);
+  const bool rtc = T > (size_t)kDecodeMaxT;  // batches routed by the tensor-core screen
+  ws.wr16 = (uint16_t*)take(rtc ? 2 * E * H * 2 : 0);
+  ws.wrnorm = (float*)take(rtc ? E * 4 : 0);
+  ws.sapprox = (float*)take(rtc ? T * E * 4 : 0);
   ws.total = off;
   return ws;
 }

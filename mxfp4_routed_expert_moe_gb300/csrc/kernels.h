@@ -1,6 +1,8 @@
 // kernels.h — host-side launchers of the library's kernels (one per stage).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -45,6 +47,20 @@ inline void prof_before(int stage, cudaStream_t s) {
 inline void prof_after(int stage, cudaStream_t s) {
   if (g_prof.after[stage]) cudaEventRecord(g_prof.after[stage], s);
 }
+
+// cuTensorMapEncodeTiled from the driver (looked up once through the
+// runtime); null if unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// route_tc.cu
+// Router scores of a bf16 batch above 64 tokens on tensor cores (a screen)
+// plus exact double-float scores of the experts that can reach the top k,
+// into ws.logits (the others get -inf); cudaErrorNotSupported for a shape it
+// does not take (the caller then runs the CUDA-core GEMM).
+cudaError_t launch_router_tc(const RouteParams& p, cudaStream_t s);
 
 // route.cu
 bool route_decode_supported(int T, int H, int E, int k);

@@ -1612,11 +1612,6 @@ __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, cons
 
 bool prefill_supported(int H, int I) { return H % 128 == 0 && I % 128 == 0; }
 
-namespace {
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (no link-time dependency on the driver library); null if unavailable.
 EncodeTiledFn encode_tiled_fn() {
@@ -1631,6 +1626,8 @@ EncodeTiledFn encode_tiled_fn() {
   });
   return fn;
 }
+
+namespace {
 
 // Tensor map of the f16 h rows [rows][I] for the down GEMM's token tiles:
 // boxes of 64 elements (128 bytes) x 128 rows, 128-byte swizzle (the MMA's

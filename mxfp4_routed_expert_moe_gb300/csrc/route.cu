@@ -551,12 +551,18 @@ cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cu
   const int nsplit = router_splits(p.T, p.E, p.H);
   const dim3 g1((p.E + kGmTE - 1) / kGmTE, (p.T + kGmTT - 1) / kGmTT, nsplit);
   prof_before(MOE_STAGE_ROUTE, s);
-  if (p.x_bf16)
-    k_router_gemm<true><<<g1, 256, 0, s>>>(p);
-  else
-    k_router_gemm<false><<<g1, 256, 0, s>>>(p);
-  cudaError_t err = cudaGetLastError();
-  if (err == cudaSuccess && nsplit > 1) {
+  // bf16 batches: the tensor-core screen with exact scores for the candidates
+  // (route_tc.cu); otherwise the CUDA-core GEMM for every score.
+  cudaError_t err = launch_router_tc(p, s);
+  const bool screened = err == cudaSuccess;
+  if (err == cudaErrorNotSupported) {
+    if (p.x_bf16)
+      k_router_gemm<true><<<g1, 256, 0, s>>>(p);
+    else
+      k_router_gemm<false><<<g1, 256, 0, s>>>(p);
+    err = cudaGetLastError();
+  }
+  if (err == cudaSuccess && !screened && nsplit > 1) {
     const size_t n = (size_t)p.T * p.E;
     const size_t cap = (size_t)device_sm_count() * 8;
     const int grid = (int)((n + 255) / 256 < cap ? (n + 255) / 256 : cap);

@@ -42,6 +42,14 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M >> 4
 }
 
+// Instruction descriptor, kind::f16: A = B = bf16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (1u << 7) | (1u << 10)        // A, B format: bf16
+         | ((uint32_t)(N >> 3) << 17)    // N >> 3
+         | ((uint32_t)(M >> 4) << 24);   // M >> 4
+}
+
 // Instruction descriptor, kind::mxf8f6f4 with UE8M0 block scales (one scale
 // per 32 elements of K): A and B K-major, D = f32.  Formats: E4M3 = 0,
 // E5M2 = 1, E2M3 = 3, E3M2 = 4, E2M1 = 5.  a_sf / b_sf select the byte of the

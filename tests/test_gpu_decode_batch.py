@@ -153,14 +153,36 @@ def test_decode_batch_bad_pair_entry_is_flagged():
 
 
 def test_router_split_contraction_routes():
-    """The router GEMM splits its contraction when the batch has few tiles
-    (here 16 splits: 100 tokens, 64 experts, H = 4096) and adds the splits'
+    """The CUDA-core router GEMM (the tensor-core screen takes H % 64 == 0,
+    so H = 4128 runs on it) splits its contraction when the batch has few
+    tiles (here 16 splits: 100 tokens, 64 experts) and adds the splits'
     double-float partial sums in order; routes, weights and buckets match the
     oracle, with a per-expert bias."""
     from harness import check_buckets
-    wl = synth.Workload("split_router", 100, 4096, 64, 8, 128)
+    wl = synth.Workload("split_router", 100, 4128, 64, 8, 128)
     inp = synth.make_inputs(wl, seed=8)
     inp.br = (np.arange(wl.E, dtype=np.float32) % 7 - 3.0) * 0.05
+    L = DeviceLayer(inp)
+    ids, w, off, srt = L.route()
+    torch().cuda.synchronize()
+    assert L.status() == 0
+    ids, w, off, srt = (a.cpu().numpy() for a in (ids, w, off, srt))
+    check_route(inp, ids, w)
+    check_buckets(ids, off, srt, wl.E)
+
+
+@pytest.mark.parametrize("T,H,E", [(100, 4096, 64), (333, 1024, 200), (70, 512, 2048)],
+                         ids=["T100_E64", "T333_E200_ragged", "T70_E2048"])
+def test_router_screen_routes(T, H, E):
+    """Batches above 64 tokens (bf16) are routed by the tensor-core screen
+    plus exact scores for the candidate experts: routes and weights match the
+    oracle (ids exact up to near-ties of the exact arithmetic), buckets are a
+    stable sort, with a per-expert bias; ragged token and expert tiles, and
+    2048 experts."""
+    from harness import check_buckets
+    wl = synth.Workload(f"screen_T{T}_E{E}", T, H, E, 16 if E >= 16 else 8, 128)
+    inp = synth.make_inputs(wl, seed=31)
+    inp.br = (np.arange(wl.E, dtype=np.float32) % 11 - 5.0) * 0.03
     L = DeviceLayer(inp)
     ids, w, off, srt = L.route()
     torch().cuda.synchronize()
@@ -185,16 +207,17 @@ def test_decode_path_with_shared_expert(T):
     assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-3
 
 
-def test_prefill_workload_auto_takes_decode_path_with_shared_expert():
-    """The 512-token layer with the shared expert: the automatic choice runs
-    the routed experts on the decode path and the shared expert on the
-    prefill kernels; sampled tokens against the oracle."""
+def test_prefill_workload_decode_path_with_shared_expert():
+    """The 512-token layer with the shared expert on the decode path (the
+    automatic choice takes the prefill path at about 9 routed pairs per
+    expert): the routed experts on the decode kernels, the shared expert on
+    the prefill kernels; sampled tokens against the oracle."""
     import mxfp4_routed_expert_moe_gb300 as moe
     wl = synth.WORKLOADS["prefill"]
-    assert moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, shared=True) == moe.PATH_DECODE
+    assert moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, shared=True) == moe.PATH_PREFILL
     inp = synth.make_inputs(wl)
     L = DeviceLayer(inp)
-    out, ids, w = L.forward()
+    out, ids, w = L.forward(path=moe.PATH_DECODE)
     torch().cuda.synchronize()
     assert L.status() == 0
     _, same = check_route(inp, ids.cpu().numpy(), w.cpu().numpy())
