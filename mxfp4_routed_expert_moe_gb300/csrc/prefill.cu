@@ -1098,9 +1098,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const
 //     count rounded up to 32: one of four maps);
 //   * 4 scale warps (one per TMEM lane quarter) write the rows' scale words
 //     (4 bytes = the slice's four blocks) into the stage's scale columns;
-//   * one thread issues the MMAs (4 K-steps x matrices x terms, M = 128,
+//   * one thread per matrix issues its MMAs (4 K-steps x terms, M = 128,
 //     N = round16(tokens), K = 32; the terms share one read of A through the
-//     A collector) and releases the stage with tcgen05.commit;
+//     A collector) and releases the stage with tcgen05.commit: a block-scaled
+//     MMA costs its issuing thread about 60 cycles whatever N is, so gate/up
+//     issues from two threads (3.58 -> 2.74 ms on the 4096-token workload);
 //   * 4 epilogue warps read one of two accumulator buffers while the MMAs fill
 //     the other: gate/up apply SwiGLU with the token's 2^-tau and store h in
 //     fp32 (with each h row's largest |h|); down adds w * 2^-tau * y into out
@@ -1117,7 +1119,7 @@ constexpr int kXMaps = 4;                        // box heights 32, 64, 96, 128
 constexpr int kTmaWarp = 1;                      // warp 0: MMA issuer, owns TMEM
 constexpr int kSfWarp0 = 2, kSfWarps = 4;        // warps 2-5
 constexpr int kEpWarp0 = kSfWarp0 + kSfWarps, kEpWarps = 4;  // warps 6-9
-constexpr int kThreads = (kEpWarp0 + kEpWarps) * 32;
+constexpr int kMma2Warp = kEpWarp0 + kEpWarps;                 // warp 10: gate/up's second issuer (up)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
 }  // namespace mxk
@@ -1132,6 +1134,8 @@ constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
 template <bool GU>
 struct MxCfg {
   static constexpr int NA = GU ? 2 : 1;                   // weight matrices per item
+  static constexpr int NI = GU ? 2 : 1;                   // MMA-issuing threads (one per matrix)
+  static constexpr int THREADS = (mxk::kMma2Warp + NI - 1) * 32;
   static constexpr int NT = GU ? 2 : 3;                   // activation terms
   static constexpr int N = GU ? kPfNTileGu : kPfNTile;    // tokens per tile (at most)
   static constexpr int XROWS = (N + mxk::kXBox - 1) / mxk::kXBox * mxk::kXBox;
@@ -1400,8 +1404,9 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_
 // were written by tensor-map copies (async proxy), so no proxy fence is
 // needed.
 template <bool GU>
-__device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem) {
+__device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem, int which) {
   using C = MxCfg<GU>;
+  constexpr int MPI = C::NA / C::NI;  // matrices this issuer covers
   MxShared<GU>& sh = *c.sh;
   int ci = 0, gs = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
@@ -1427,7 +1432,8 @@ __device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t 
       for (int kb = 0; kb < 4; ++kb) {
         const uint32_t idesc = ibase | ((uint32_t)kb << 29) | ((uint32_t)kb << 4);
 #pragma unroll
-        for (int a = 0; a < C::NA; ++a) {
+        for (int m = 0; m < MPI; ++m) {
+          const int a = which * MPI + m;
           const uint64_t ad = sdesc_sw128(sbase + a * mxk::kTile + 32 * kb);
           const uint32_t d = tmem + (uint32_t)b * C::AccW + (uint32_t)(a * C::N);
           const uint32_t sfa = tmem + C::ColSfa + (uint32_t)(4 * (C::NA * st + a));
@@ -1556,7 +1562,7 @@ __device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx<GU>& c, uint
 }
 
 template <bool GU>
-__global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, const __grid_constant__ MxXMaps xmaps) {
+__global__ void __launch_bounds__(MxCfg<GU>::THREADS, 1) k_pf_mx(ExpertParams p, const __grid_constant__ MxXMaps xmaps) {
   using C = MxCfg<GU>;
   extern __shared__ uint8_t mx_dyn[];
   __shared__ MxShared<GU> sh;
@@ -1568,10 +1574,10 @@ __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sh.full[s], 1 + mxk::kSfWarps);
-      mbar_init(&sh.empty[s], 1);
+      mbar_init(&sh.empty[s], C::NI);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sh.accf[b], 1);
+      mbar_init(&sh.accf[b], C::NI);
       mbar_init(&sh.acce[b], mxk::kEpWarps);
     }
     sh.abort_flag = 0;
@@ -1592,8 +1598,9 @@ __global__ void __launch_bounds__(mxk::kThreads, 1) k_pf_mx(ExpertParams p, cons
   c.srow = K / 32;
   c.hdr = p.ws.hdr;
   c.wait_limit = p.wait_limit;
-  if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) mx_mma_role<GU>(p, c, tmem);
+  if (warp == 0 || warp == mxk::kMma2Warp) {
+    const int which = warp == 0 ? 0 : 1;
+    if ((threadIdx.x & 31) == 0 && which < C::NI) mx_mma_role<GU>(p, c, tmem, which);
   } else if (warp == mxk::kTmaWarp) {
     mx_producer_role<GU>(p, c, &xmaps);
   } else if (warp < mxk::kEpWarp0) {
@@ -1750,7 +1757,7 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
   ExpertParams ps = p;  // the shared expert's items alone
   ps.shared_only = 1;
   prof_before(MOE_STAGE_PF_GATEUP, s);
-  if (routed) k_pf_mx<true><<<nsm, mxk::kThreads, mxgu_smem, s>>>(p, xmaps);
+  if (routed) k_pf_mx<true><<<nsm, MxCfg<true>::THREADS, mxgu_smem, s>>>(p, xmaps);
   if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
     k_pf_gemm<true><<<nsm, kPfThreads, gu_smem, s>>>(ps, tmap_h);
     err = cudaGetLastError();
@@ -1768,7 +1775,7 @@ cudaError_t launch_prefill_experts(const ExpertParams& p, cudaStream_t s) {
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   prof_before(MOE_STAGE_PF_DOWN, s);
-  if (routed) k_pf_mx<false><<<nsm, mxk::kThreads, mxdn_smem, s>>>(p, hmaps);
+  if (routed) k_pf_mx<false><<<nsm, MxCfg<false>::THREADS, mxdn_smem, s>>>(p, hmaps);
   if ((err = cudaGetLastError()) == cudaSuccess && p.sh_gate) {
     k_pf_gemm<false><<<nsm, kPfThreads, dn_smem, s>>>(ps, tmap_h);
     err = cudaGetLastError();
