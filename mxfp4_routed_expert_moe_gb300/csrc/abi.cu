@@ -87,7 +87,7 @@ BucketParams bucket_params(const moe_shape* s, const int32_t* ids, int32_t* offs
   b.ids = ids;
   b.offsets_out = offsets_out;
   b.sorted_out = sorted_out;
-  b.n_tile = kPfNTile;
+  b.n_tile = kPfNTileDn;
   b.n_tile_gu = kPfNTileGu;
   b.m_tiles_gu = (s->I + kPfMTile - 1) / kPfMTile;
   b.m_tiles_dn = (s->H + kPfMTile - 1) / kPfMTile;

@@ -71,9 +71,10 @@ struct Ws {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Tokens per tile of the prefill path's block-scaled gate/up GEMM (two
-// accumulator buffers of gate + up columns fit Tensor Memory).
+// Tokens per tile of the prefill path's block-scaled GEMMs (two accumulator
+// buffers of two accumulators each fit Tensor Memory next to the scales).
 constexpr int kPfNTileGu = 112;
+constexpr int kPfNTileDn = 96;
 
 // Splits of the contraction of the router GEMM (64 experts x 64 tokens per
 // CTA) for batches above 64 tokens (smaller ones keep their workspace size;
@@ -118,7 +119,7 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
     // tile of up to 128), then the shared expert's tiles.  The token tiles of
     // all active experts number at most ceil(T*k/128) + min(E, T*k).
     const size_t pairs = T * k;
-    const size_t ntiles = (pairs + 127) / 128 + (E < pairs ? E : pairs);
+    const size_t ntiles = (pairs + kPfNTileDn - 1) / kPfNTileDn + (E < pairs ? E : pairs);
     const size_t ntiles_gu = (pairs + kPfNTileGu - 1) / kPfNTileGu + (E < pairs ? E : pairs);
     const size_t shtiles = (T + 127) / 128;
     const size_t mgu = (I + 127) / 128, mdn = (H + 127) / 128;
@@ -364,7 +365,7 @@ struct BucketParams {
   const int32_t* ids;      // [T][k]
   int32_t* offsets_out;    // [E+1] caller copy or NULL
   int32_t* sorted_out;     // [T*k] caller copy or NULL
-  int n_tile;              // prefill token tile (columns of one MMA tile): down GEMM
+  int n_tile;              // prefill token tile (columns of one MMA tile) of the routed down GEMM
   int n_tile_gu;           // prefill token tile of the routed gate/up GEMM
   int m_tiles_gu;          // prefill row tiles of gate/up (ceil(I/128))
   int m_tiles_dn;          // prefill row tiles of down (ceil(H/128))

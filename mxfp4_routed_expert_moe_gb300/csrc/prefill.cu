@@ -324,8 +324,9 @@ __global__ void __launch_bounds__(256) k_shared_sigma(ExpertParams p) {
 // ------------------------------------------------------------ work items --
 // Items are (expert, 128-row weight tile, token tile).  Routed items come
 // first, active experts in ascending order, row tiles outer; then the shared
-// expert's items when there is one.  Token tiles hold up to 128 tokens, the
-// routed gate/up items (block-scaled GEMM) up to kPfNTileGu.
+// expert's items when there is one.  The shared expert's token tiles hold up
+// to 128 tokens, the routed items (block-scaled GEMMs) up to kPfNTileGu
+// (gate/up) or kPfNTileDn (down).
 struct PfItem {
   int shared;  // 1: the bf16 shared expert
   int e;       // routed expert
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(256) k_pf_items(ExpertParams p) {
     if (w <= U)
       pf_fill_items(p, p.ws.act_pref_gu, p.ws.items_gu, p.I, w, U, kPfNTileGu);
     else
-      pf_fill_items(p, p.ws.act_pref_dn, p.ws.items_dn, p.H, w - U - 1, U, kPfNTile);
+      pf_fill_items(p, p.ws.act_pref_dn, p.ws.items_dn, p.H, w - U - 1, U, kPfNTileDn);
   }
 }
 
@@ -1098,11 +1099,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(ExpertParams p, const
 //     count rounded up to 32: one of four maps);
 //   * 4 scale warps (one per TMEM lane quarter) write the rows' scale words
 //     (4 bytes = the slice's four blocks) into the stage's scale columns;
-//   * one thread per matrix issues its MMAs (4 K-steps x terms, M = 128,
-//     N = round16(tokens), K = 32; the terms share one read of A through the
-//     A collector) and releases the stage with tcgen05.commit: a block-scaled
-//     MMA costs its issuing thread about 60 cycles whatever N is, so gate/up
-//     issues from two threads (3.58 -> 2.74 ms on the 4096-token workload);
+//   * two threads issue the MMAs (K-steps x terms, M = 128, N =
+//     round16(tokens), K = 32; the terms share one read of A through the A
+//     collector), each into its own accumulator (gate/up: one matrix each;
+//     down: two of the four K-steps each), and release the stage with
+//     tcgen05.commit: a block-scaled MMA costs its issuing thread about 60
+//     cycles whatever N is (4096-token workload: gate/up 3.58 -> 2.74 ms,
+//     down 2.93 -> 2.65 ms with the second issuer);
 //   * 4 epilogue warps read one of two accumulator buffers while the MMAs fill
 //     the other: gate/up apply SwiGLU with the token's 2^-tau and store h in
 //     fp32 (with each h row's largest |h|); down adds w * 2^-tau * y into out
@@ -1125,23 +1128,25 @@ constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
 }  // namespace mxk
 
 // Per GEMM: a stage holds the NA weight tiles and an activation box of up to
-// N rows (rounded up to 32) of each of the NT terms: 64 KB, three stages
-// (gate/up: N = 112; down: N = 128).  A fourth stage with 96-token gate/up
-// tiles was slower: more items outweighed the deeper ring.  TMEM columns: two
-// accumulator buffers of AccW columns (matrix a at a * N of the buffer); the
-// terms' constant scales (4 columns each) at ColSfb; the weight scales of
-// stage st, matrix a at ColSfa + 4 (NA st + a).
+// N rows (rounded up to 32) of each of the NT terms (gate/up: N = 112, three
+// 64 KB stages; down: N = 96, four 52 KB stages; a fourth gate/up stage with
+// 96-token tiles was slower, more items outweighing the deeper ring).  Two
+// threads issue the MMAs, each into an accumulator of its own: gate/up one
+// matrix each, down two of a slice's four K-steps each (the epilogue adds the
+// two).  TMEM columns: two buffers of AccW columns (accumulator i at i * N of
+// the buffer); the terms' constant scales (4 columns each) at ColSfb; the
+// weight scales of stage st, matrix a at ColSfa + 4 (NA st + a).
 template <bool GU>
 struct MxCfg {
   static constexpr int NA = GU ? 2 : 1;                   // weight matrices per item
-  static constexpr int NI = GU ? 2 : 1;                   // MMA-issuing threads (one per matrix)
+  static constexpr int NI = 2;                            // MMA-issuing threads, one accumulator each
   static constexpr int THREADS = (mxk::kMma2Warp + NI - 1) * 32;
   static constexpr int NT = GU ? 2 : 3;                   // activation terms
-  static constexpr int N = GU ? kPfNTileGu : kPfNTile;    // tokens per tile (at most)
+  static constexpr int N = GU ? kPfNTileGu : kPfNTileDn;  // tokens per tile (at most)
   static constexpr int XROWS = (N + mxk::kXBox - 1) / mxk::kXBox * mxk::kXBox;
   static constexpr int STAGE = NA * mxk::kTile + NT * XROWS * 128;
-  static constexpr int STAGES = 3;
-  static constexpr uint32_t AccW = NA * N;
+  static constexpr int STAGES = GU ? 3 : 4;
+  static constexpr uint32_t AccW = NI * N;
   static constexpr uint32_t ColSfb = 2 * AccW;
   static constexpr uint32_t ColSfa = ColSfb + 4 * NT;
   static_assert(ColSfa + 4 * NA * STAGES <= mxk::kTmemCols, "TMEM columns");
@@ -1406,7 +1411,11 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_
 template <bool GU>
 __device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem, int which) {
   using C = MxCfg<GU>;
-  constexpr int MPI = C::NA / C::NI;  // matrices this issuer covers
+  // gate/up: matrix `which`, all four K-steps of a slice; down: matrix 0,
+  // K-steps 2 which and 2 which + 1.  Accumulator `which` either way.
+  const int a = GU ? which : 0;
+  constexpr int KB = GU ? 4 : 2;
+  const int kb0 = GU ? 0 : 2 * which;
   MxShared<GU>& sh = *c.sh;
   int ci = 0, gs = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
@@ -1428,26 +1437,23 @@ __device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t 
       tc_fence_after();
       const uint32_t sbase = smem_u32(c.ring + (size_t)st * C::STAGE);
       const uint32_t xbase = sbase + C::NA * mxk::kTile;
+      const uint32_t d = tmem + (uint32_t)b * C::AccW + (uint32_t)(which * C::N);
+      const uint32_t sfa = tmem + C::ColSfa + (uint32_t)(4 * (C::NA * st + a));
 #pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
+      for (int i = 0; i < KB; ++i) {
+        const int kb = kb0 + i;
         const uint32_t idesc = ibase | ((uint32_t)kb << 29) | ((uint32_t)kb << 4);
+        const uint64_t ad = sdesc_sw128(sbase + a * mxk::kTile + 32 * kb);
 #pragma unroll
-        for (int m = 0; m < MPI; ++m) {
-          const int a = which * MPI + m;
-          const uint64_t ad = sdesc_sw128(sbase + a * mxk::kTile + 32 * kb);
-          const uint32_t d = tmem + (uint32_t)b * C::AccW + (uint32_t)(a * C::N);
-          const uint32_t sfa = tmem + C::ColSfa + (uint32_t)(4 * (C::NA * st + a));
-#pragma unroll
-          for (int j = 0; j < C::NT; ++j) {
-            const uint64_t bd = sdesc_sw128(xbase + j * xstep + 32 * kb);
-            const uint32_t sfb = tmem + C::ColSfb + 4u * j;
-            if (j == 0)
-              umma_mx_fill(d, ad, bd, idesc, sfa, sfb, (s > 0 || kb > 0) ? 1u : 0u);
-            else if (j < C::NT - 1)
-              umma_mx_use(d, ad, bd, idesc, sfa, sfb, 1u);
-            else
-              umma_mx_lastuse(d, ad, bd, idesc, sfa, sfb, 1u);
-          }
+        for (int j = 0; j < C::NT; ++j) {
+          const uint64_t bd = sdesc_sw128(xbase + j * xstep + 32 * kb);
+          const uint32_t sfb = tmem + C::ColSfb + 4u * j;
+          if (j == 0)
+            umma_mx_fill(d, ad, bd, idesc, sfa, sfb, (s > 0 || i > 0) ? 1u : 0u);
+          else if (j < C::NT - 1)
+            umma_mx_use(d, ad, bd, idesc, sfa, sfb, 1u);
+          else
+            umma_mx_lastuse(d, ad, bd, idesc, sfa, sfb, 1u);
         }
       }
       umma_commit(&sh.empty[st]);
@@ -1541,13 +1547,15 @@ __device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx<GU>& c, uint
         }
         if (lane < 16 && c0 + lane < it.cnt && habs != 0u) atomicMax(&p.ws.hmax[it.hpos0 + c0 + lane], habs);
       } else {
+        uint32_t g2[16];  // the second issuer's accumulator (K-steps 2 and 3)
+        tmem_ld16(tbase + (uint32_t)C::N + (uint32_t)c0, g2);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = c0 + i;
             if (n < it.cnt) {
-              float v = __uint_as_float(g[i]) * col_scale[n];
+              float v = (__uint_as_float(g[i]) + __uint_as_float(g2[i])) * col_scale[n];
               if (nan_row) v = __int_as_float(0x7FC00000);
               atomicAdd(&p.out[(size_t)col_tok[n] * p.H + row], v);
             }
@@ -1599,8 +1607,7 @@ __global__ void __launch_bounds__(MxCfg<GU>::THREADS, 1) k_pf_mx(ExpertParams p,
   c.hdr = p.ws.hdr;
   c.wait_limit = p.wait_limit;
   if (warp == 0 || warp == mxk::kMma2Warp) {
-    const int which = warp == 0 ? 0 : 1;
-    if ((threadIdx.x & 31) == 0 && which < C::NI) mx_mma_role<GU>(p, c, tmem, which);
+    if ((threadIdx.x & 31) == 0) mx_mma_role<GU>(p, c, tmem, warp == 0 ? 0 : 1);
   } else if (warp == mxk::kTmaWarp) {
     mx_producer_role<GU>(p, c, &xmaps);
   } else if (warp < mxk::kEpWarp0) {
