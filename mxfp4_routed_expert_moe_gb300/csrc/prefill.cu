@@ -1139,15 +1139,20 @@ constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollSf = 64, kPollEp = 256;
 template <bool GU>
 struct MxCfg {
   static constexpr int NA = GU ? 2 : 1;                   // weight matrices per item
-  static constexpr int NI = 2;                            // MMA-issuing threads, one accumulator each
-  static constexpr int THREADS = (mxk::kMma2Warp + NI - 1) * 32;
   static constexpr int NT = GU ? 2 : 3;                   // activation terms
   static constexpr int N = GU ? kPfNTileGu : kPfNTileDn;  // tokens per tile (at most)
   static constexpr int XROWS = (N + mxk::kXBox - 1) / mxk::kXBox * mxk::kXBox;
   static constexpr int STAGE = NA * mxk::kTile + NT * XROWS * 128;
   static constexpr int STAGES = GU ? 3 : 4;
+  // MMA-issuing threads, one accumulator each (four gate/up issuers, which
+  // leave room for a single accumulator buffer only, were slower: 2.79 ->
+  // 3.29 ms on the 4096-token workload).
+  static constexpr int NI = 2;
+  static constexpr int ACCB = NI * N * 2 + 4 * NT + 4 * NA * STAGES <= 512 ? 2 : 1;  // accumulator buffers
+  static constexpr int KB = 4 * NA / NI;                  // K-steps of a slice per issuer
+  static constexpr int THREADS = (mxk::kMma2Warp + NI - 1) * 32;
   static constexpr uint32_t AccW = NI * N;
-  static constexpr uint32_t ColSfb = 2 * AccW;
+  static constexpr uint32_t ColSfb = ACCB * AccW;
   static constexpr uint32_t ColSfa = ColSfb + 4 * NT;
   static_assert(ColSfa + 4 * NA * STAGES <= mxk::kTmemCols, "TMEM columns");
   static_assert(STAGES <= mxk::kMaxStages && STAGE % 1024 == 0, "stages");
@@ -1411,16 +1416,16 @@ __device__ void mx_scale_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_
 template <bool GU>
 __device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t tmem, int which) {
   using C = MxCfg<GU>;
-  // gate/up: matrix `which`, all four K-steps of a slice; down: matrix 0,
-  // K-steps 2 which and 2 which + 1.  Accumulator `which` either way.
-  const int a = GU ? which : 0;
-  constexpr int KB = GU ? 4 : 2;
-  const int kb0 = GU ? 0 : 2 * which;
+  // Issuer `which` takes matrix which / (NI / NA) and KB consecutive K-steps
+  // of each slice, into accumulator `which`.
+  constexpr int KB = C::KB;
+  const int a = which / (C::NI / C::NA);
+  const int kb0 = (which % (C::NI / C::NA)) * KB;
   MxShared<GU>& sh = *c.sh;
   int ci = 0, gs = 0;
   for (int item = blockIdx.x; item < c.n_items; item += gridDim.x, ++ci) {
     const PfItem it = pf_item(item, p, c.items);
-    const int b = ci & 1, use = ci >> 1;
+    const int b = ci % C::ACCB, use = ci / C::ACCB;
     if (use >= 1 && !mx_wait(c, &sh.acce[b], (use - 1) & 1, mxk::kPollMma)) break;
     tc_fence_after();
     const int nmma = (it.cnt + 15) & ~15;
@@ -1465,7 +1470,8 @@ __device__ void mx_mma_role(const ExpertParams& p, const MxCtx<GU>& c, uint32_t 
     }
   }
   // Every MMA issued must have finished before TMEM is released.
-  if (ci > 0 && !mbar_wait(&sh.accf[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) set_status(c.hdr, MOE_ERR_TIMEOUT);
+  if (ci > 0 && !mbar_wait(&sh.accf[(ci - 1) % C::ACCB], ((ci - 1) / C::ACCB) & 1))
+    set_status(c.hdr, MOE_ERR_TIMEOUT);
 }
 
 // Epilogue warps: warp q reads TMEM lanes 32q..32q+31 (weight rows m0 + 32q +
@@ -1519,16 +1525,28 @@ __device__ void mx_epilogue_role(const ExpertParams& p, const MxCtx<GU>& c, uint
       }
     }
     __syncwarp();
-    const int b = ci & 1;
-    if (!mx_warp_wait(c, &sh.accf[b], (ci >> 1) & 1, mxk::kPollEp)) break;
+    const int b = ci % C::ACCB;
+    if (!mx_warp_wait(c, &sh.accf[b], (ci / C::ACCB) & 1, mxk::kPollEp)) break;
     tc_fence_after();
     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * C::AccW;
+    constexpr int PER = C::NI / C::NA;  // accumulators per matrix (added here)
     for (int c0 = 0; c0 < it.cnt; c0 += 16) {
       uint32_t g[16];
       tmem_ld16(tbase + (uint32_t)c0, g);
       if (GU) {
         uint32_t u[16];
-        tmem_ld16(tbase + (uint32_t)C::N + (uint32_t)c0, u);
+        tmem_ld16(tbase + (uint32_t)(PER * C::N) + (uint32_t)c0, u);
+        if (PER == 2) {
+          uint32_t g2[16], u2[16];
+          tmem_ld16(tbase + (uint32_t)C::N + (uint32_t)c0, g2);
+          tmem_ld16(tbase + (uint32_t)(3 * C::N) + (uint32_t)c0, u2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            g[i] = __float_as_uint(__uint_as_float(g[i]) + __uint_as_float(g2[i]));
+            u[i] = __float_as_uint(__uint_as_float(u[i]) + __uint_as_float(u2[i]));
+          }
+        }
         tmem_ld_wait();
         uint32_t habs = 0u;
 #pragma unroll
@@ -1606,8 +1624,9 @@ __global__ void __launch_bounds__(MxCfg<GU>::THREADS, 1) k_pf_mx(ExpertParams p,
   c.srow = K / 32;
   c.hdr = p.ws.hdr;
   c.wait_limit = p.wait_limit;
-  if (warp == 0 || warp == mxk::kMma2Warp) {
-    if ((threadIdx.x & 31) == 0) mx_mma_role<GU>(p, c, tmem, warp == 0 ? 0 : 1);
+  if (warp == 0 || warp >= mxk::kMma2Warp) {
+    // Issuer 0 is warp 0 (it owns TMEM); issuers 1.. are warps kMma2Warp...
+    if ((threadIdx.x & 31) == 0) mx_mma_role<GU>(p, c, tmem, warp == 0 ? 0 : warp - mxk::kMma2Warp + 1);
   } else if (warp == mxk::kTmaWarp) {
     mx_producer_role<GU>(p, c, &xmaps);
   } else if (warp < mxk::kEpWarp0) {
