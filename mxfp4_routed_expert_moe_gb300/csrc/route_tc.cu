@@ -9,8 +9,9 @@
 //      mid = bf16(W - hi), so |W - hi - mid| <= 2^-16 |W|; the Euclidean norm
 //      of each row, rounded up; clears the per-expert token masks.
 //   2. k_router_tc: s~ = x (hi + mid)^T + b on tensor cores (kind::f16, bf16
-//      operands, fp32 accumulation in Tensor Memory over the whole
-//      contraction), 128-token x 128-expert tiles fed by tensor-map copies.
+//      operands), 128-token x 128-expert tiles fed by tensor-map copies; the
+//      MMAs accumulate chunks of kChunk slices in Tensor Memory (alternating
+//      two buffers), and the epilogue adds the chunks in fp32 registers.
 //   3. k_router_exact, one CTA per token: a bound B(e) on |s~ - s|, the k-th
 //      largest lower bound L = kth_e(s~ - B), and the candidates {e :
 //      s~ + B >= L}, which include every expert of the true top k; their
@@ -25,8 +26,10 @@
 //     accumulator; taking its error as at most 18 units of 2^-23 of the sum
 //     of the magnitudes of its 17 addends (alignment and truncation of every
 //     addend plus a final rounding, a worst-case model of the tensor core's
-//     fp32 sum), the 2H/16 MMAs of a score err by at most
-//     18 2^-23 (H/8 + 1) (1 + 2^-7) S;
+//     fp32 sum), a chunk of M MMAs errs by at most 18 2^-23 (M + 1) S_chunk,
+//     so all chunks together by 18 2^-23 (M + 1) (1 + 2^-7) S, with
+//     M = 8 min(kChunk, H / 64) (8 MMAs per 64-element slice); adding the C
+//     chunks in fp32 registers errs by at most C 2^-24 (1 + 2^-7) S;
 //   * the fp32 addition of the bias: at most 2^-24 (|s~| + |b|).
 // B(e) adds these with the norms rounded up by 2^-9 and a further 2^-22 of
 // (|s~| + B) for the rounding of s~ -+ B themselves.
@@ -51,8 +54,17 @@ constexpr int kThreads = 192;               // warp 0 MMA issuer (owns TMEM), wa
 constexpr uint32_t kTmemCols = 256;         // two accumulator buffers of 128 columns
 constexpr int kExactThreads = 256;
 constexpr int kMaxE = 4096;
+constexpr int kChunk = 14;                  // slices per accumulation chunk (896 elements)
 constexpr uint32_t kPollMma = 0, kPollTma = 32, kPollEp = 128;
 }  // namespace rtc
+
+// Coefficient of S in the bound (see the file comment).
+__device__ __forceinline__ float rtc_alpha(int H) {
+  const int ns = H / rtc::kSliceK;
+  const int per_chunk = (ns < rtc::kChunk ? ns : rtc::kChunk) * 2 * (rtc::kSliceK / 16);  // MMAs
+  const int chunks = (ns + rtc::kChunk - 1) / rtc::kChunk;
+  return 0x1p-16f + (18.f * 0x1p-23f * (float)(per_chunk + 1) + 0x1p-24f * (float)chunks) * (1.f + 1.f / 128.f);
+}
 
 // ------------------------------------------------------------------ prep --
 // One warp per expert row.
@@ -188,15 +200,23 @@ __global__ void __launch_bounds__(rtc::kThreads, 1)
         if (issued[i] >= 0 && !mbar_wait(&sh.full[i], issued[i] & 1)) set_status(hdr, MOE_ERR_TIMEOUT);
   } else if (warp == 0) {
     if (lane == 0) {
-      // MMA issuer.
+      // MMA issuer: chunk cc (global over the CTA's items) goes to buffer
+      // cc & 1, which the epilogue has drained since its use two chunks ago.
       const uint32_t idesc = idesc_bf16_f32(rtc::kTile, rtc::kTile);
-      int ci = 0, gs = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ci) {
-        const int b = ci & 1, use = ci >> 1;
-        if (use >= 1 && !rtc_wait(sh, &sh.acce[b], (use - 1) & 1, hdr, rtc::kPollMma, lim)) break;
-        tc_fence_after();
-        bool ok = true;
+      int cc = 0, gs = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        int b = 0;
         for (int s = 0; s < ns; ++s, ++gs) {
+          if (s % rtc::kChunk == 0) {
+            b = cc & 1;
+            const int use = cc >> 1;
+            if (use >= 1 && !rtc_wait(sh, &sh.acce[b], (use - 1) & 1, hdr, rtc::kPollMma, lim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           const int st = gs % rtc::kStages;
           if (!rtc_wait(sh, &sh.full[st], (gs / rtc::kStages) & 1, hdr, rtc::kPollMma, lim)) {
             ok = false;
@@ -211,45 +231,64 @@ __global__ void __launch_bounds__(rtc::kThreads, 1)
             for (int term = 0; term < 2; ++term)
               umma_f16(tmem + (uint32_t)(b * rtc::kTile), ad,
                        sdesc_sw128(sbase + (uint32_t)((1 + term) * rtc::kTileBytes) + 32 * kb), idesc,
-                       (s > 0 || kb > 0 || term > 0) ? 1u : 0u);
+                       (s % rtc::kChunk > 0 || kb > 0 || term > 0) ? 1u : 0u);
           }
           umma_commit(&sh.empty[st]);
-        }
-        umma_commit(&sh.accf[b]);
-        if (!ok) {
-          ++ci;
-          break;
-        }
-      }
-      if (ci > 0 && !mbar_wait(&sh.accf[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) set_status(hdr, MOE_ERR_TIMEOUT);
-    }
-  } else {
-    // Epilogue warps 2-5: TMEM lane quarter q = warp % 4, token t0 + 32 q + lane.
-    const int q = warp & 3;
-    int ci = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ci) {
-      const int t0 = (item / etiles) * rtc::kTile, e0 = (item % etiles) * rtc::kTile;
-      const int b = ci & 1;
-      bool got = rtc_wait(sh, &sh.accf[b], (ci >> 1) & 1, hdr, rtc::kPollEp, lim);
-      if (!__all_sync(0xFFFFFFFFu, got)) break;
-      tc_fence_after();
-      const int t = t0 + q * 32 + lane;
-      float* dst = p.ws.sapprox + (size_t)t * p.E;
-      for (int c0 = 0; c0 < rtc::kTile; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * rtc::kTile + c0), v);
-        tmem_ld_wait();
-        if (t < p.T) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int e = e0 + c0 + j;
-            if (e < p.E) dst[e] = __uint_as_float(v[j]) + (p.br ? __ldg(&p.br[e]) : 0.f);
+          if (s % rtc::kChunk == rtc::kChunk - 1 || s == ns - 1) {
+            umma_commit(&sh.accf[b]);
+            ++cc;
           }
         }
+        if (!ok && ns > 0 && gs % rtc::kChunk != 0) {
+          // A chunk broken off: commit it so that the drain below waits for it.
+          umma_commit(&sh.accf[b]);
+          ++cc;
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.acce[b]);
+      if (cc > 0 && !mbar_wait(&sh.accf[(cc - 1) & 1], ((cc - 1) >> 1) & 1)) set_status(hdr, MOE_ERR_TIMEOUT);
+    }
+  } else {
+    // Epilogue warps 2-5: TMEM lane quarter q = warp % 4, token t0 + 32 q +
+    // lane; the item's chunks are added in fp32 registers in chunk order.
+    const int q = warp & 3;
+    const int nchunks = (ns + rtc::kChunk - 1) / rtc::kChunk;
+    int cc = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int t0 = (item / etiles) * rtc::kTile, e0 = (item % etiles) * rtc::kTile;
+      float acc[rtc::kTile];
+#pragma unroll
+      for (int j = 0; j < rtc::kTile; ++j) acc[j] = 0.f;
+      for (int ch = 0; ch < nchunks; ++ch, ++cc) {
+        const int b = cc & 1;
+        bool got = rtc_wait(sh, &sh.accf[b], (cc >> 1) & 1, hdr, rtc::kPollEp, lim);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < rtc::kTile; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * rtc::kTile + c0), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c0 + j] += __uint_as_float(v[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.acce[b]);
+      }
+      if (!ok) break;
+      const int t = t0 + q * 32 + lane;
+      if (t < p.T) {
+        float* dst = p.ws.sapprox + (size_t)t * p.E;
+#pragma unroll
+        for (int j = 0; j < rtc::kTile; ++j) {
+          const int e = e0 + j;
+          if (e < p.E) dst[e] = acc[j] + (p.br ? __ldg(&p.br[e]) : 0.f);
+        }
+      }
     }
   }
   tc_fence_before();
@@ -302,8 +341,7 @@ __global__ void __launch_bounds__(rtc::kExactThreads) k_router_exact(RouteParams
     xnorm = sqrtf(tot) * (1.f + 1.f / 512.f);
   }
   __syncthreads();
-  // alpha: the split (2^-16) plus the accumulation (18 2^-23 (H/8 + 1) (1 + 2^-7)).
-  const float alpha = 0x1p-16f + 18.f * 0x1p-23f * (float)(H / 8 + 1) * (1.f + 1.f / 128.f);
+  const float alpha = rtc_alpha(H);
   const float xn = xnorm;
   const float* sa_row = p.ws.sapprox + (size_t)t * E;
   for (int e = tid; e < E; e += rtc::kExactThreads) {
