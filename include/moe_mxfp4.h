@@ -128,7 +128,15 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 typedef enum {
   MOE_PATH_AUTO = 0,
   MOE_PATH_DECODE = 1,
-  MOE_PATH_PREFILL = 2
+  MOE_PATH_PREFILL = 2,
+  /* The decode step as one persistent kernel on block-scaled tensor-core
+   * MMAs (the E2M1 codes and E8M0 scales read by the MMA as stored): routing,
+   * gate/up + SwiGLU, down and the slot-ordered combine in one launch after
+   * the router scores.  bf16 x, T <= 8, H and I multiples of 128, I >= 256,
+   * I <= 2048.  Never chosen automatically: measured on GB300 at the
+   * pages' layer shape it is slower than MOE_PATH_DECODE (0.140 against
+   * 0.091 ms at 1 token, 0.43 against 0.41 ms at 8 tokens). */
+  MOE_PATH_DECODE_MX = 3
 } moe_path;
 
 #define MOE_DECODE_MAX_T 64
@@ -145,7 +153,7 @@ uint32_t moe_abi_version(void);
 
 /* The path a call with this shape, activation type, shared expert (0 / 1)
  * and `path` argument runs, without running it: *path_out receives
- * MOE_PATH_DECODE or MOE_PATH_PREFILL.  Returns the status the call would
+ * MOE_PATH_DECODE, MOE_PATH_PREFILL or (when requested) MOE_PATH_DECODE_MX.  Returns the status the call would
  * return for these arguments before launching (MOE_ERR_INVALID_ARG for a bad
  * shape, enum or null path_out; MOE_ERR_UNSUPPORTED when the requested path
  * cannot take them).  Host only; no CUDA call. */

@@ -30,6 +30,7 @@ DT_BF16 = 1
 PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_PREFILL = 2
+PATH_DECODE_MX = 3  # the persistent block-scaled decode kernel (explicit choice only)
 DECODE_MAX_T = 64                  # MOE_DECODE_MAX_T
 DECODE_BATCH_MAX_T = 1024          # MOE_DECODE_BATCH_MAX_T
 DECODE_AUTO_PAIRS_PER_EXPERT = 5  # MOE_DECODE_AUTO_PAIRS_PER_EXPERT

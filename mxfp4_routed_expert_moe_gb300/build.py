@@ -12,8 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_mxfp4.so")
-SOURCES = ["abi.cu", "route.cu", "route_tc.cu", "decode.cu", "prefill.cu"]
-HEADERS = ["common.cuh", "kernels.h", "async.cuh", "route_small.cuh", "tcgen05.cuh"]
+SOURCES = ["abi.cu", "route.cu", "route_tc.cu", "decode.cu", "decode_mx.cu", "prefill.cu"]
+HEADERS = ["common.cuh", "kernels.h", "async.cuh", "route_small.cuh", "tcgen05.cuh", "decode_mx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC] + ARCH

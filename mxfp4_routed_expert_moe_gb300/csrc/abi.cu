@@ -73,6 +73,9 @@ int resolve_path(const moe_shape* s, int x_dtype, bool has_shared, int path, int
     if (has_shared && (x_dtype != MOE_DT_BF16 || !prefill_supported(s->H, s->I))) return MOE_ERR_UNSUPPORTED;
   } else if (path == MOE_PATH_PREFILL) {
     if (x_dtype != MOE_DT_BF16 || !prefill_supported(s->H, s->I)) return MOE_ERR_UNSUPPORTED;
+  } else if (path == MOE_PATH_DECODE_MX) {
+    if (x_dtype != MOE_DT_BF16 || !dmx_shape_supported(s->T, s->H, s->E, s->I, s->k)) return MOE_ERR_UNSUPPORTED;
+    if (has_shared && !prefill_supported(s->H, s->I)) return MOE_ERR_UNSUPPORTED;
   } else {
     return MOE_ERR_INVALID_ARG;
   }
@@ -108,6 +111,7 @@ RouteParams route_params(const moe_shape* s, const void* x, int x_dtype, const f
   p.offsets = offsets;
   p.sorted = sorted;
   p.want_buckets = 1;
+  p.dmx_I = 0;
   p.wait_limit = g_wait_limit;
   p.ws = ws;
   return p;
@@ -126,6 +130,7 @@ int do_route(const moe_shape* s, const void* x, int x_dtype, const float* wr, co
   p.offsets = offsets;
   p.sorted = sorted;
   p.want_buckets = 1;
+  p.dmx_I = 0;
   p.wait_limit = g_wait_limit;
   p.ws = ws;
   if (want_decode_route && route_decode_supported(s->T, s->H, s->E, s->k)) return cuda_status(launch_route_decode(p, st));
@@ -158,6 +163,11 @@ ExpertParams expert_params(const moe_shape* s, const void* x, int x_dtype, const
 }
 
 int run_experts(const ExpertParams& p, int path, cudaStream_t st) {
+  if (path == MOE_PATH_DECODE_MX) {
+    if (p.sh_gate) return MOE_ERR_UNSUPPORTED;
+    if (!dmx_supported(p)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_dec_mx(p, st));
+  }
   if (path == MOE_PATH_DECODE) {
     if (p.sh_gate) return MOE_ERR_UNSUPPORTED;
     return cuda_status(launch_decode_experts(p, st));
@@ -304,9 +314,11 @@ int moe_forward(const moe_shape* shape, const void* x, int x_dtype, const float*
   float* w = w_out ? w_out : L.w;
   if ((st = cuda_status(cudaMemsetAsync(L.hdr, 0, sizeof(WsHeader), s))) != MOE_OK) return st;
   const ExpertParams p = expert_params(shape, x, x_dtype, experts, ids, w, L.offsets, L.sorted, out, accumulate, shared, L);
-  if (rpath == MOE_PATH_DECODE) {
+  if (rpath == MOE_PATH_DECODE || rpath == MOE_PATH_DECODE_MX) {
     const RouteParams rp = route_params(shape, x, x_dtype, w_router, b_router, ids, w, nullptr, nullptr, L);
-    st = cuda_status(launch_decode_forward(rp, bucket_params(shape, ids, nullptr, nullptr, L), p, s));
+    if (rpath == MOE_PATH_DECODE_MX && !dmx_supported(p)) return MOE_ERR_UNSUPPORTED;
+    st = cuda_status(launch_decode_forward(rp, bucket_params(shape, ids, nullptr, nullptr, L), p, s,
+                                           rpath == MOE_PATH_DECODE_MX));
     if (st != MOE_OK || !shared) return st;
     // The shared expert: the prefill GEMM kernels with no routed items (the
     // active-expert count cleared), adding its output into out.

@@ -66,6 +66,11 @@ struct Ws {
   float* wrnorm;        // [E] Euclidean norm of each router row, rounded up (T > 64 only)
   float* sapprox;       // [T][E] tensor-core approximation of the router scores (T > 64 only)
   uint32_t* rowdone;    // [ceil(H/32)] per-row-tile completion counters
+  // Persistent block-scaled decode kernel (T <= 8; empty otherwise):
+  uint8_t* dmx_xq;      // [16][H] the tokens' E4M3 terms (rows 2t, 2t + 1)
+  uint8_t* dmx_hq;      // [3 T k][I] h of each routed pair (bucket order) as three E4M3 terms
+  uint8_t* dmx_hs;      // [3 T k][I / 32] E8M0 scale of each 32-element block of those rows
+  uint32_t* dmx_cnt;    // counters (see dmx_counter_words)
   size_t total;
 };
 
@@ -90,6 +95,25 @@ __host__ __device__ inline int router_splits(int T, int E, int H) {
   s = s < smax ? s : smax;
   s = s < 16 ? s : 16;
   return s < 1 ? 1 : s;
+}
+
+// Persistent block-scaled decode kernel (decode_mx.cu): batch and tile limits.
+constexpr int kDmxMaxT = 8;        // tokens of a step the kernel takes
+constexpr int kDmxNGu = 16;        // gate/up B rows: two E4M3 terms of each of up to 8 tokens
+constexpr int kDmxNDn = 32;        // down B rows: three E4M3 terms of each of up to 8 pairs (+ padding)
+constexpr int kDmxCntHead = 32;     // counter words before the per-tile counters
+
+// Shapes whose workspace holds the kernel's buffers.
+__host__ __device__ inline bool dmx_shape_ok(int T, int H, int I) {
+  return T >= 1 && T <= kDmxMaxT && H >= 128 && H % 128 == 0 && I >= 256 && I % 128 == 0;
+}
+// Gate/up slices (128 elements) whose scale words the persistent decode
+// kernel stages at a time: the smallest divisor of the slice count that is
+// at least 12 (or all of them; at most 16).
+__host__ __device__ inline int dmx_spp(int ns) {
+  for (int d = 12; d < ns; ++d)
+    if (ns % d == 0) return d;
+  return ns;
 }
 
 // Layout of the workspace for a shape; pointers are offsets from `base`.
@@ -156,6 +180,16 @@ inline Ws ws_layout(const moe_shape& s, void* base) {
   ws.xp = (uint8_t*)ws.y;
   ws.h8 = (uint8_t*)ws.y + h8_off;
   ws.rowdone = (uint32_t*)take(((H + 31) / 32) * 4);
+  {
+    // The persistent block-scaled decode kernel's buffers.
+    const bool dmx = dmx_shape_ok(s.T, s.H, s.I);
+    const size_t rt = I / 128;
+    const size_t umax = E < T * k ? E : T * k;
+    ws.dmx_xq = (uint8_t*)take(dmx ? (size_t)kDmxNGu * H : 0);
+    ws.dmx_hq = (uint8_t*)take(dmx ? 3 * T * k * I : 0);
+    ws.dmx_hs = (uint8_t*)take(dmx ? 3 * T * k * (I / 32) : 0);
+    ws.dmx_cnt = (uint32_t*)take(dmx ? (kDmxCntHead + umax * rt) * 4 : 0);
+  }
   const size_t S = (size_t)router_splits(s.T, s.E, s.H);
   ws.rpart = (float2*)take(S > 1 ? S * T * E * 8 : 0);
   const bool rtc = T > (size_t)kDecodeMaxT;  // batches routed by the tensor-core screen
@@ -354,6 +388,7 @@ struct RouteParams {
   int32_t* offsets;     // bucket outputs (may alias workspace)
   int32_t* sorted;
   int want_buckets;
+  int dmx_I;             // > 0: the router kernel also prepares the persistent decode kernel (intermediate size)
   long long wait_limit;  // cycles before a bounded wait gives up (kWaitCycles unless diagnosing)
   Ws ws;
 };

@@ -1997,9 +1997,23 @@ static cudaError_t launch_decode_nt(const ExpertParams& p, cudaStream_t s) {
 // The whole decode layer: router scores, then (when the staged kernels apply)
 // gate/up with the routing fused into its prologue and down + combine;
 // otherwise the standalone routing kernels and the register-streaming path.
-cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s) {
+// With mx: the router scores, then the persistent block-scaled kernel.
+cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s,
+                                  bool mx) {
   const bool small_route = route_decode_supported(rp.T, rp.H, rp.E, rp.k);
   const bool staged = p.T == 1 ? tma_path_ok<1>(p) : tma_path_ok<2>(p);
+  if (mx) {
+    if (!small_route || !dmx_supported(p)) return cudaErrorNotSupported;
+    // Router scores (and the E4M3 activation terms), then the persistent
+    // block-scaled kernel routes and runs every routed expert.
+    RouteParams r2 = rp;
+    r2.dmx_I = p.I;
+    cudaError_t err = launch_router_gemv(r2, s);
+    if (err != cudaSuccess) return err;
+    p.fused_route = 1;
+    p.rp = r2;
+    return launch_dec_mx(p, s);
+  }
   if (small_route && staged) {
     cudaError_t err = launch_router_gemv(rp, s);
     if (err != cudaSuccess) return err;

@@ -54,6 +54,20 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
+// Template of the per-expert code maps of the block-scaled GEMMs: an [M][K]
+// matrix of 4-bit codes, boxes of 128 elements x 128 rows (prefill.cu).
+cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int K, int M);
+
+// decode_mx.cu
+// Whether the persistent block-scaled decode kernel takes this call (bf16,
+// T <= 8, 128 | H, 128 | I, I >= 256, the device's SM count and shared memory).
+bool dmx_supported(const ExpertParams& p);
+// The shape part of dmx_supported (host, no device query).
+bool dmx_shape_supported(int T, int H, int E, int I, int k);
+// The routed experts of a decode step in one launch (routing first when
+// p.fused_route; otherwise from the published buckets, after a preparation
+// kernel).
+cudaError_t launch_dec_mx(const ExpertParams& p, cudaStream_t s);
 
 // route_tc.cu
 // Router scores of a bf16 batch above 64 tokens on tensor cores (a screen)
@@ -79,7 +93,8 @@ cudaError_t launch_copy_pairs(const int32_t* in, int32_t* out, int npairs, WsHea
 // decode path of batches above 64 tokens runs only on them).
 bool decode_batch_supported(int T, int H, int E, int I, int k);
 cudaError_t launch_decode_experts(const ExpertParams& p, cudaStream_t s);
-cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s);
+cudaError_t launch_decode_forward(const RouteParams& rp, const BucketParams& bp, ExpertParams p, cudaStream_t s,
+                                  bool mx = false);
 
 // prefill.cu
 constexpr int kPfNTile = 128;   // tokens per MMA tile (N)

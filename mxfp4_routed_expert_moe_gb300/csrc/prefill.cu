@@ -1677,23 +1677,6 @@ cudaError_t encode_h16_map(CUtensorMap* m, void* base, int rows, int I) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-// Template of the per-expert code maps of the block-scaled GEMMs: an [M][K]
-// matrix of 4-bit codes (row stride K / 2 bytes), boxes of 128 elements x 128
-// rows, each 16 codes stored as 8 bytes followed by an 8-byte gap, 128-byte
-// swizzle.  `base` only has to be a valid 32-byte-aligned address:
-// k_pf_mx_maps replaces it per expert.
-cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int K, int M) {
-  const EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-  const cuuint32_t box[2] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)kPfMTile};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
 
 // Map of bucket-order E4M3 activation rows as a [terms][T k][K] byte tensor
 // (term, row, byte): boxes of 128 bytes x `rows` rows x all terms, 128-byte
@@ -1712,6 +1695,24 @@ cudaError_t encode_terms_map(CUtensorMap* m, void* base, int npairs, int K, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 }  // namespace
+
+// Template of the per-expert code maps of the block-scaled GEMMs: an [M][K]
+// matrix of 4-bit codes (row stride K / 2 bytes), boxes of 128 elements x 128
+// rows, each 16 codes stored as 8 bytes followed by an 8-byte gap, 128-byte
+// swizzle.  `base` only has to be a valid 32-byte-aligned address:
+// the kernels replace it per expert.
+cudaError_t encode_code_map_template(CUtensorMap* m, void* base, int K, int M) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+  const cuuint32_t box[2] = {(cuuint32_t)mxk::kSliceK, (cuuint32_t)kPfMTile};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 template <bool GATEUP>
 constexpr size_t pf_smem_bytes() {

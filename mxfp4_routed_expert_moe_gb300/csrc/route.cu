@@ -12,6 +12,7 @@
 
 #include "async.cuh"
 #include "kernels.h"
+#include "decode_mx.cuh"
 #include "route_small.cuh"
 
 namespace moe {
@@ -117,14 +118,18 @@ __global__ void __launch_bounds__(kRgThreads) k_router_gemv(RouteParams p) {
   }
   pdl_trigger();
   // The decode expert kernels read the activations as f16 with a per-token
-  // shift: CTA b converts tokens b, b + gridDim.x, .. (bf16 input) while its
-  // copy lands.
-  if (XBF16)
+  // shift, or (the persistent block-scaled kernel) as E4M3 terms with its
+  // counters cleared: CTA b converts tokens b, b + gridDim.x, .. (bf16 input)
+  // while its copy lands.
+  if (XBF16 && p.dmx_I > 0) {
+    dmx_prepare(p.x, T, H, E, p.dmx_I, p.k, p.ws, blockIdx.x, gridDim.x);
+  } else if (XBF16) {
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
       x_row_to_f16(reinterpret_cast<const uint16_t*>(p.x) + (size_t)t * H, H, p.ws.xh + (size_t)t * H,
                    &p.ws.xscale[t]);
       __syncthreads();  // x_row_to_f16 reuses its shared maxima
     }
+  }
   __syncthreads();
   bool rows_ready = false;
   for (int tp = 0; tp < T; tp += 2) {

@@ -196,6 +196,7 @@ struct SmallPlan {
   int* ub0;     // [umax] bucket offset
   int* un;      // [umax] bucket size
   int* pairs;   // [T*k]  routed pairs t*k+j grouped by expert, ascending inside
+  float* wts = nullptr;  // [T*k] the pairs' weights (optional; filled by every CTA)
 };
 
 constexpr int kRouteWarps = 8;  // warps that route tokens (one token per warp at a time)
@@ -262,6 +263,7 @@ static __device__ void route_small(const RouteParams& p, char* scratch, SmallPla
           p.w[t * k + lane] = wt;
         }
         s_ids[t * k + lane] = my_e;
+        if (plan.wts) plan.wts[t * k + lane] = wt;
         atomicOr(&tmask[my_e], 1ull << t);
       }
     }
