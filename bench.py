@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill"],
+    ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "decode_mx"],
                     help="expert path of the workload (default: the library's own choice)")
     ap.add_argument("--no-prefill-leg", action="store_true",
                     help="with the default 1-token decode workload, skip the 4096-token prefill leg")
@@ -212,7 +212,14 @@ class Layer:
     def decode_path(self) -> bool:
         wl, moe = self.wl, self.moe
         dt = moe.DT_F32 if wl.x_dtype == "f32" else moe.DT_BF16
-        return moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, dt, self.shared is not None, self.path) == moe.PATH_DECODE
+        return moe.select_path(wl.T, wl.H, wl.E, wl.I, wl.k, dt, self.shared is not None,
+                               self.path) in (moe.PATH_DECODE, moe.PATH_DECODE_MX)
+
+    @property
+    def persistent_decode(self) -> bool:
+        """The explicit persistent block-scaled decode kernel (routing, gate/up,
+        down and combine in one launch after the router)."""
+        return self.path == self.moe.PATH_DECODE_MX
 
     def launches_per_step(self) -> int:
         # prefill: router GEMM, top-k, bucket count, bucket scatter, pair positions, x->E4M3 rows,
@@ -222,6 +229,8 @@ class Layer:
             # shared expert: x->fp16, its row shifts, item tables, and the two prefill GEMMs (with
             # the h->fp16 pass between them) on its tiles alone
             sh = 6 if self.shared is not None else 0
+            if self.persistent_decode:
+                return 2 + sh  # router (+ E4M3 activation terms, counters), the persistent kernel
             if self.wl.T <= self.moe.DECODE_MAX_T:
                 return 3 + sh  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
             # router, top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
@@ -651,7 +660,7 @@ def sweep(args, device):
 
 
 # --------------------------------------------------------------------- main --
-PATHS = {"auto": None, "decode": 1, "prefill": 2}
+PATHS = {"auto": None, "decode": 1, "prefill": 2, "decode_mx": 3}
 
 
 def step_stats(step_ms):
@@ -715,7 +724,14 @@ def measure(layer, args, rank, world, local, device, steps, cpu_seconds, parity_
     e2e_ms = time_e2e(layer, max(20, min(steps, 200)), 3, graph)
     breakdown = stage_breakdown(layer)
     nograph_ms = statistics.mean(time_steps(layer, 50 if wl.T <= 64 else 10, 3, False)[0]) if not args.no_graph else ms
-    if layer.decode_path:
+    if layer.decode_path and layer.persistent_decode:
+        # One launch streams every routed expert's gate, up and down weights.
+        ex_bytes = n_active * wl.expert_bytes
+        achieved = ex_bytes / (st_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "kernel": "k_dec_mx (persistent block-scaled decode: routing, gate/up, down, combine)",
+                "bytes_per_launch": ex_bytes, "launch_ms": st_ms, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
+    elif layer.decode_path:
         gu_bytes = layer.algorithmic_bytes_gateup(n_active)
         achieved = gu_bytes / (st_ms / 1000.0) / 1e9
         traffic, sha = traffic_from_profiles("dec_gateup", wl.name)
