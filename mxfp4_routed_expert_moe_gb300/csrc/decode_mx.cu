@@ -27,10 +27,11 @@
 //
 // Roles of a CTA (one per SM): warps 0 and 10 (lane 0) issue the MMAs
 // (accumulator 0: gate rows / even down slices; accumulator 1: up rows / odd
-// down slices; warp 0 owns Tensor Memory); warps 1 and 11 copy the code
-// boxes, warps 12 and 13 the B tiles (even and odd stages): the copy unit
-// serves the copies of one issuing thread one after another, so one thread
-// cannot keep the stream busy; warps 2-5 stage the block scales and write
+// down slices; warp 0 owns Tensor Memory); warps 1, 11, 14 and 15 copy the
+// code boxes (box 0 or 1 of the even or the odd stages), warps 12 and 13 the
+// B tiles (even and odd stages): the copy unit serves the copies of one
+// issuing thread one after another, so one thread cannot keep the stream
+// busy; warps 2-5 stage the block scales and write
 // them into Tensor Memory; warps 6-9 drain the accumulators.  Gate/up tiles
 // are dealt to the CTAs in waves, so each expert's h is finished early;
 // down items go mostly to the CTAs with one gate/up tile fewer, so the weight
