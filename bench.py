@@ -760,7 +760,7 @@ def measure(layer, args, rank, world, local, device, steps, cpu_seconds, parity_
         "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s", "ms_per_step": ms,
         "step_ms_stats": stats,
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
-                   "x_dtype": wl.x_dtype, "path": "decode" if layer.decode_path else "prefill",
+                   "x_dtype": wl.x_dtype, "path": ("decode_mx" if layer.persistent_decode else "decode") if layer.decode_path else "prefill",
                    "path_arg": args.path, "cuda_graph": not args.no_graph,
                    "l2": "flushed before every step (256 MiB write, then 256 MiB read; outside the step timing)",
                    "active_experts": n_active, "parallelism": f"replicas x{world}"},
