@@ -222,8 +222,8 @@ class Layer:
         return self.path == self.moe.PATH_DECODE_MX
 
     def launches_per_step(self) -> int:
-        # prefill: router GEMM, top-k, bucket count, bucket scatter, pair positions, x->E4M3 rows,
-        # item tables, code maps, block-scaled gate/up, h->E4M3, block-scaled down; the shared
+        # prefill: routing (see _router_launches), bucket count, bucket scatter, pair positions,
+        # x->E4M3 rows, item tables, code maps, block-scaled gate/up, h->E4M3, block-scaled down; the shared
         # expert adds x->fp16, its row shifts, its gate/up, h->fp16 and its down
         if self.decode_path:
             # shared expert: x->fp16, its row shifts, item tables, and the two prefill GEMMs (with
@@ -233,18 +233,18 @@ class Layer:
                 return 2 + sh  # router (+ E4M3 activation terms, counters), the persistent kernel
             if self.wl.T <= self.moe.DECODE_MAX_T:
                 return 3 + sh  # router (+ f16 activations), gate/up (+ fused top-k/bucketing), down (+ fused combine)
-            # router, top-k, bucket count, bucket scatter, x->fp16, gate/up, down, combine
-            return 7 + self._router_launches() + sh
-        return 10 + self._router_launches() + (5 if self.shared is not None else 0)
+            # routing (below), bucket count, bucket scatter, x->fp16, gate/up, down, combine
+            return 6 + self._router_launches() + sh
+        return 9 + self._router_launches() + (5 if self.shared is not None else 0)
 
     def _router_launches(self) -> int:
-        """Router kernels of a batch above 64 tokens: the tensor-core screen (W split, screen
-        GEMM, exact candidate scores) for bf16 x, H % 64 == 0 and E <= 4096; else the CUDA-core
-        GEMM (and its split reduction)."""
+        """Routing kernels of a batch above 64 tokens: the tensor-core screen (W split, screen
+        GEMM, exact candidate scores with the top-k) for bf16 x, H % 64 == 0 and E <= 4096; else
+        the CUDA-core GEMM (and its split reduction) and the top-k."""
         wl = self.wl
         if wl.x_dtype != "f32" and wl.H % 64 == 0 and wl.E <= 4096:
             return 3
-        return 1 + (1 if self._router_splits() > 1 else 0)
+        return 1 + (1 if self._router_splits() > 1 else 0) + 1
 
     def _router_splits(self) -> int:
         """Splits of the router GEMM's contraction (the library's rule)."""

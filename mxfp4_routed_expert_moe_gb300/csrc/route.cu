@@ -576,11 +576,13 @@ cudaError_t launch_route_prefill(const RouteParams& p, const BucketParams& b, cu
   }
   prof_after(MOE_STAGE_ROUTE, s);
   if (err != cudaSuccess) return err;
-  const size_t smem = (size_t)8 * p.E * 8;
-  err = ensure_smem_attr((const void*)k_topk, smem);
-  if (err != cudaSuccess) return err;
-  k_topk<<<(p.T + 7) / 8, 256, smem, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (!screened) {  // the screen selects the top k itself
+    const size_t smem = (size_t)8 * p.E * 8;
+    err = ensure_smem_attr((const void*)k_topk, smem);
+    if (err != cudaSuccess) return err;
+    k_topk<<<(p.T + 7) / 8, 256, smem, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
   k_bucket_count<<<(p.E + 7) / 8, 256, 0, s>>>(b);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   k_bucket_scatter<<<(p.T * p.k + 255) / 256, 256, 0, s>>>(b);

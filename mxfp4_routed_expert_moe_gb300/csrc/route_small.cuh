@@ -66,6 +66,58 @@ __device__ __forceinline__ void warp_topk(float2* row, int E, int k, int& my_e, 
   }
 }
 
+// Top-k of one token by one warp over a list of n scored experts (sc[c] the
+// double-float score of expert id[c]; sc is destroyed): larger score first,
+// lower expert index on equal scores; lane j < k returns slot j's expert and
+// score.  Entry c belongs to lane c % 32.
+__device__ __forceinline__ void warp_topk_list(float2* sc, const int* id, int n, int k, int& my_e, float2& my_s) {
+  const int lane = threadIdx.x & 31;
+  my_e = -1;
+  my_s = make_float2(0.f, 0.f);
+  auto scan = [&](unsigned long long& best, int& best_e, int& best_c) {
+    best = 0ull;
+    best_e = 0x7FFFFFFF;
+    best_c = -1;
+    for (int c = lane; c < n; c += 32) {
+      const unsigned long long kk = score_key(sc[c]);
+      const int e = id[c];
+      if (kk > best || (kk == best && kk != 0ull && e < best_e)) {
+        best = kk;
+        best_e = e;
+        best_c = c;
+      }
+    }
+  };
+  unsigned long long lb;
+  int le, lc;
+  scan(lb, le, lc);
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = lb;
+    int best_e = le, best_c = lc;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, m);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, best_e, m);
+      const int oc = __shfl_xor_sync(0xFFFFFFFFu, best_c, m);
+      if (ok > best || (ok == best && oe < best_e)) {
+        best = ok;
+        best_e = oe;
+        best_c = oc;
+      }
+    }
+    if (lane == j && best_c >= 0) {
+      my_e = best_e;
+      my_s = sc[best_c];
+    }
+    __syncwarp();
+    if (best_c >= 0 && (best_c & 31) == lane) {  // the winner's lane takes it out and rescans
+      sc[best_c].x = __uint_as_float(kTaken);
+      scan(lb, le, lc);
+    }
+    __syncwarp();
+  }
+}
+
 // ---- small-batch top-k on packed keys (E <= 4096) ----
 // key = ord(hi) << 32 | (ord(lo) with its low 12 bits replaced by 4095 - e):
 // value order first (hi, then the top 20 bits of lo, far below any score

@@ -17,8 +17,9 @@
 //      s~ + B >= L}, which include every expert of the true top k; their
 //      scores are computed exactly as the CUDA-core GEMM does (fp32 products
 //      summed in chunks of 16, chunk sums carried in double-float, the bias
-//      added in double-float), the others are set to -inf, and k_topk then
-//      selects from the exact scores.
+//      added in double-float), and the kernel selects the top k among them,
+//      writes their renormalised weights and sets the token's mask bits (the
+//      other experts' scores are never needed).
 //
 // The bound.  With S = sum_h |x_h| |W_eh| <= ||x|| ||W_e|| (Cauchy-Schwarz):
 //   * the split: |sum x (W - hi - mid)| <= 2^-16 S;
@@ -359,18 +360,23 @@ __global__ void __launch_bounds__(rtc::kExactThreads) k_router_exact(RouteParams
   }
   __syncthreads();
   const float L = kth;
-  float2* logits = p.ws.logits + (size_t)t * E;
   for (int e = tid; e < E; e += rtc::kExactThreads) {
     const float sa = sa_row[e];
     const float bias = p.br ? __ldg(&p.br[e]) : 0.f;
     const float B = rtc_bound(sa, bias, xn * __ldg(&p.ws.wrnorm[e]), alpha);
-    if (sa + B >= L)
-      cand[atomicAdd(&ncand, 1)] = e;
-    else
-      logits[e] = make_float2(-INFINITY, 0.f);
+    if (sa + B >= L) cand[atomicAdd(&ncand, 1)] = e;
   }
   __syncthreads();
+  if (ncand < k) {
+    // Only non-finite scores leave fewer than k candidates: every expert is one.
+    __syncthreads();
+    if (tid == 0) ncand = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += rtc::kExactThreads) cand[atomicAdd(&ncand, 1)] = e;
+    __syncthreads();
+  }
   const int nc = ncand;
+  float2* csc = row;  // the candidates' exact scores, in candidate order (the bounds are done)
   for (int c = warp; c < nc; c += rtc::kExactThreads / 32) {
     const int e = cand[c];
     const float* w = p.wr + (size_t)e * H;
@@ -402,7 +408,22 @@ __global__ void __launch_bounds__(rtc::kExactThreads) k_router_exact(RouteParams
     if (lane == 0) {
       float sh, sl;
       df_add(hi, lo, p.br ? __ldg(&p.br[e]) : 0.f, 0.f, sh, sl);
-      logits[e] = make_float2(sh, sl);
+      csc[c] = make_float2(sh, sl);
+    }
+  }
+  __syncthreads();
+  // The top k among the candidates (they include the true top k), their
+  // renormalised weights, and the token's bit in each selected expert's mask.
+  if (warp == 0) {
+    int my_e;
+    float2 my_s;
+    warp_topk_list(csc, cand, nc, k, my_e, my_s);
+    const float wt = warp_route_weight(my_s, k);
+    if (lane < k) {
+      p.ids[(size_t)t * k + lane] = my_e;
+      p.w[(size_t)t * k + lane] = wt;
+      const int W = (p.T + 31) / 32;
+      atomicOr(&p.ws.mask[(size_t)my_e * W + (t >> 5)], 1u << (t & 31));
     }
   }
 }
