@@ -3,7 +3,6 @@
 // synchronises except moe_device_status().
 #include <string.h>
 
-#include <mutex>
 
 #include "async.cuh"
 #include "kernels.h"
@@ -179,21 +178,13 @@ int run_experts(const ExpertParams& p, int path, cudaStream_t st) {
 // device memory (one instance per device), so that call allocates nothing.
 static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (with that device current).
+// Device address of g_static_scratch in the current context, looked up on
+// every call: a cached address would go stale after cudaDeviceReset or under
+// another context on the same device.
 int static_scratch_ptr(void** out) {
-  constexpr int kMaxDevices = 64;
-  static void* table[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!table[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    table[dev] = p;
-  }
-  *out = table[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+  *out = p;
   return MOE_OK;
 }
 
