@@ -80,6 +80,23 @@ def test_route_rejects_bad_arguments_before_launch(moe):
     assert _call_route(moe, big, x=A, wr=A, ids=A, w=A, ws=A, ws_bytes=1 << 30) == moe.MOE_ERR_UNSUPPORTED
 
 
+def test_degenerate_shapes_are_rejected_before_launch(moe):
+    """An empty batch, k = 0, k > E and H off the 32-element MX block grid are
+    invalid shapes (the header's limits): no workspace size, and every entry
+    point returns MOE_ERR_INVALID_ARG without touching its (fake) pointers."""
+    L = moe.lib()
+    A = 1 << 20
+    for T, H, E, I, k in [(0, 256, 8, 128, 2), (4, 256, 8, 128, 0), (4, 256, 8, 128, 9), (4, 240, 8, 128, 2),
+                          (4, 256, 8, 112, 2), (4, 256, 0, 128, 1)]:
+        shp = moe.shape(T, H, E, I, k)
+        assert L.moe_workspace_bytes(ctypes.byref(shp)) == 0, (T, H, E, I, k)
+        assert _call_route(moe, shp, x=A, wr=A, ids=A, w=A, ws=A, ws_bytes=1 << 30) == moe.MOE_ERR_INVALID_ARG
+        rc = L.moe_forward(ctypes.byref(shp), A, 1, A, None, A, None, A, 0, None, None, 0, A, 1 << 30, None)
+        assert rc == moe.MOE_ERR_INVALID_ARG
+        rc = L.moe_mxfp4_experts(ctypes.byref(shp), A, 1, A, A, A, None, None, A, 0, 0, A, 1 << 30, None)
+        assert rc == moe.MOE_ERR_INVALID_ARG
+
+
 def test_forward_and_experts_reject_bad_arguments(moe):
     L = moe.lib()
     A = 1 << 20
